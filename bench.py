@@ -1,0 +1,421 @@
+"""Benchmark of the paged KV-injection hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of requests of the
+Llama-3-8B-shaped workload (32 layers, 32 q / 8 kv heads, d 128, bf16,
+block 16, batch 32, contexts U[512, 2048], 8 injected chunks of 64 tokens per
+request from a resident pool of 4096 pre-RoPE chunks, 1 decode step):
+
+    slot mapping -> inject (gather, RoPE, scatter; all layers) ->
+    per layer: append the new token's K/V, paged GQA decode attention
+
+The headline `value` is the step's algorithmic HBM traffic (bytes the step
+must move at minimum: injected chunk rows read and written, appended rows,
+every context K/V row read once per layer, plus q/out/block tables) divided
+by the step time, in GB/s; the injection rate (injected tokens/s) and the
+decode bandwidth are reported beside it. Inputs are resident in HBM when the
+timed region starts and larger than L2 (no flush needed); `e2e` repeats the
+measurement through the engine's host-buffer entry point with the per-step
+inputs copied from pinned host memory and the outputs copied back.
+
+--impl reference times the fp64 CPU oracle on a bounded sample (layer 0 of
+the same workload) on this machine's host cores. For N > 1 (torchrun) every
+rank runs an independent replica on its own GPU (the path has no exchange
+step); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged GQA decode HBM GB/s (% of ~8 TB/s); KV-injection tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+DEFAULT_CONFIG = "llama3_8b_b32"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:  # noqa: BLE001
+        return 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:  # noqa: BLE001
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:  # noqa: BLE001
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _traffic_from_profile(kernel_tag: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (the summary records the source hash)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.txt")
+    if not os.path.exists(path):
+        return None
+    src = _source_hash()
+    want_hash, value = None, None
+    for ln in open(path):
+        if ln.startswith("source_sha256:"):
+            want_hash = ln.split(":", 1)[1].strip()
+        if ln.startswith("dram_bytes_per_launch:"):
+            try:
+                value = float(ln.split(":", 1)[1].strip())
+            except ValueError:
+                value = None
+    return value if want_hash == src else None
+
+
+def _source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_inject_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample (cpu_baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """Layer 0 of the workload on the host: the oracle's slot mapping, inject,
+    append of the context and step tokens, and paged decode of every query
+    head of every request. Inputs are generated once (not timed)."""
+
+    def __init__(self, wl, threads: int):
+        import numpy as np
+
+        import oracle
+        self.np, self.oracle, self.wl, self.threads = np, oracle, wl, threads
+        cfg = wl.cfg
+        L0 = 0
+        Hkv, D, c = cfg.kv_heads, cfg.head_dim, cfg.chunk_len
+        ids = np.unique(wl.chunk_ids)
+        # pool rows of the drawn chunks for layer 0, as [n][1][2][c][Hkv][D]
+        pool = np.zeros((ids.size, 1, 2, c, Hkv, D), np.uint16)
+        for kv in (0, 1):
+            t = np.repeat(np.arange(c), Hkv)
+            h = np.tile(np.arange(Hkv), c)
+            for u, cid in enumerate(ids):
+                pool[u, 0, kv] = wl.pool_rows(np.full(t.size, cid), np.zeros(t.size, int),
+                                              np.full(t.size, kv), t, h).reshape(c, Hkv, D)
+        self.pool = pool
+        self.ids = np.searchsorted(ids, wl.chunk_ids).astype(np.int32)
+        self.inj_seq, self.inj_pos = wl.injected_tokens()
+        a_seq, a_pos = wl.appended_tokens()
+        s_seq, s_pos = wl.step_tokens(0)
+        self.app = [(a_seq, a_pos, wl.ctx_rows(L0, 0, a_seq, a_pos), wl.ctx_rows(L0, 1, a_seq, a_pos)),
+                    (s_seq, s_pos, wl.ctx_rows(L0, 0, s_seq, s_pos), wl.ctx_rows(L0, 1, s_seq, s_pos))]
+        self.q = wl.q_rows(0, L0)
+        self.q_pos = s_pos
+        self.ctx = s_pos + 1
+        row = Hkv * D * cfg.elem_bytes
+        n_inj_tok = wl.n_inj * c
+        n_app = sum(x[0].size for x in self.app)
+        pages = -(-self.ctx.astype(np.int64) // cfg.block_size)
+        self.bytes = (2 * 2 * row * n_inj_tok + 2 * 2 * row * n_app + int(self.ctx.sum()) * 2 * row
+                      + cfg.batch * cfg.q_heads * D * 2 * 2 + int(pages.sum()) * 4)
+        self.inj_tokens = n_inj_tok
+
+    def run(self):
+        np, orc, wl, cfg = self.np, self.oracle, self.wl, self.wl.cfg
+        shape = (1, wl.num_blocks, cfg.kv_heads, cfg.block_size, cfg.head_dim)
+        kc = np.zeros(shape, np.uint16)
+        vc = np.zeros(shape, np.uint16)
+        slots, _ = orc.slot_mapping(wl.block_tables, self.inj_seq, self.inj_pos, cfg.block_size,
+                                    wl.num_blocks)
+        orc.inject(self.pool, self.ids, wl.start_pos, slots, cfg.theta, cfg.dtype, kc, vc,
+                   n_threads=self.threads)
+        for seq, pos, kn, vn in self.app:
+            sl, _ = orc.slot_mapping(wl.block_tables, seq, pos, cfg.block_size, wl.num_blocks)
+            orc.append(kc, vc, 0, kn, vn, pos, sl, cfg.theta, cfg.dtype)
+        out, _ = orc.paged_decode(kc, vc, 0, self.q, self.q_pos, wl.block_tables, self.ctx,
+                                  cfg.theta, cfg.dtype, n_threads=self.threads)
+        return out
+
+    @property
+    def description(self):
+        cfg = self.wl.cfg
+        return (f"layer 0 of 1/{cfg.layers} layers of {cfg.name}: slot mapping, inject of "
+                f"{self.inj_tokens} tokens, append of the context and step tokens, paged decode "
+                f"of {cfg.batch}x{cfg.q_heads} query heads")
+
+
+def oracle_threads() -> int:
+    import oracle
+    return (os.cpu_count() or 1) if oracle.has_openmp() else 1
+
+
+def run_reference(args):
+    """--impl reference: the fp64 CPU oracle, as it stands, on a bounded sample."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import workload as W
+    wl = W.make_workload(W.CONFIGS[args.config])
+    threads = oracle_threads()
+    sample = OracleSample(wl, threads)
+    for _ in range(args.warmup):
+        sample.run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        sample.run()
+    dt = (time.perf_counter() - t0) / args.steps
+    gbs = sample.bytes / dt / 1e9
+    cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+           "sample": sample.description}
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.config, "sample": "layer 0"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "inject_tokens_per_s": sample.inj_tokens / dt,
+    }))
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import workload as W
+    from workload import stage
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    import __graft_entry__
+    __graft_entry__.build()
+
+    cfg = W.CONFIGS[args.config]
+    wl = W.make_workload(cfg, seed=cfg.seed + 1000 * rank)  # independent replica per rank
+    eng = stage.make_engine(wl, dev)
+    eng.decode_variant = args.variant
+    stage.fill_context(eng, wl, dev)
+    inp = stage.step_inputs(wl, dev)
+    out = eng.alloc_outputs(cfg.steps)
+    nbytes = stage.algorithmic_bytes(wl)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # warm-up (also checks the device status word)
+    for _ in range(args.warmup):
+        eng.step(inp, out)
+    torch.cuda.synchronize()
+    if eng.status.item() != 0:
+        raise RuntimeError(f"device status {eng.status.item():#x} after warm-up")
+
+    # timed region: K steps, per-kernel events on the launching stream
+    ev = {"inject": [], "decode": []}
+    pending = {}
+
+    def timer(kind, which):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        if which == 0:
+            pending[kind] = e
+        else:
+            ev[kind].append((pending.pop(kind), e))
+
+    barrier()
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for _ in range(args.steps):
+            eng.step(inp, out, timer=timer)
+        t_end.record(stream)
+        barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if ws > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_step = elapsed_ms / args.steps
+    value = ws * nbytes["total"] / (ms_step * 1e-3) / 1e9
+
+    dec_ms = [a.elapsed_time(b) for a, b in ev["decode"]]
+    inj_ms = [a.elapsed_time(b) for a, b in ev["inject"]]
+    dec_avg = sum(dec_ms) / len(dec_ms)
+    inj_avg = sum(inj_ms) / len(inj_ms)
+    per_launch_decode = nbytes["decode"] / (cfg.layers * cfg.steps)
+    dec_gbs = per_launch_decode / (dec_avg * 1e-3) / 1e9
+    inj_gbs = nbytes["inject"] / (inj_avg * 1e-3) / 1e9
+    inj_tok_s = wl.n_inj * cfg.chunk_len / (inj_avg * 1e-3)
+    peak, peak_kind = _peaks()
+    launches_per_step = 2 + 2 * cfg.layers * cfg.steps
+
+    # end to end through host buffers (pinned), same metric
+    e2e = None
+    if not args.no_e2e:
+        host = stage.pinned_copy(inp)
+        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        for _ in range(max(1, args.warmup)):
+            eng.step_from_host(host, inp, out, host_out)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            eng.step_from_host(host, inp, out, host_out)
+        e1.record(stream)
+        barrier()
+        e_ms = e0.elapsed_time(e1) / args.steps
+        if ws > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": ws * nbytes["total"] / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": e_ms, "h2d_bytes_per_step": host.nbytes,
+               "d2h_bytes_per_step": host_out.numel() * host_out.element_size()}
+    if eng.status.item() != 0:
+        raise RuntimeError(f"device status {eng.status.item():#x}")
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = oracle_threads()
+        sample = OracleSample(wl, threads)
+        t0 = time.perf_counter()
+        sample.run()
+        dt = time.perf_counter() - t0
+        cpu = {"value": sample.bytes / dt / 1e9, "unit": "GB/s", "cores": threads,
+               "kind": "oracle", "sample": sample.description, "seconds": dt}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": W.DTYPE_NAMES[cfg.dtype],
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "layers": cfg.layers, "q_heads": cfg.q_heads,
+                   "kv_heads": cfg.kv_heads, "head_dim": cfg.head_dim,
+                   "block_size": cfg.block_size, "batch": cfg.batch,
+                   "context": list(cfg.ctx), "injected_chunks_per_request": cfg.chunks_per_req,
+                   "chunk_len": cfg.chunk_len, "pool_chunks": cfg.pool_chunks,
+                   "decode_steps": cfg.steps, "parallelism": f"replicas x{ws}",
+                   "l2": (f"inputs larger than L2: {nbytes['total'] / 1e9:.2f} GB touched per "
+                          f"step; no flush"),
+                   "decode_variant": args.variant},
+        "parts": {
+            "inject": {"tokens_per_s": inj_tok_s, "gbs": inj_gbs, "ms": inj_avg,
+                       "pct_of_8tbs": 100 * inj_gbs / NOMINAL_HBM_GBS,
+                       "bytes": nbytes["inject"]},
+            "decode": {"gbs": dec_gbs, "ms_per_layer": dec_avg,
+                       "pct_of_8tbs": 100 * dec_gbs / NOMINAL_HBM_GBS,
+                       "tokens_per_s": ws * cfg.batch * cfg.steps / (ms_step * 1e-3),
+                       "bytes_per_launch": per_launch_decode},
+            "step_bytes": nbytes,
+        },
+        "roofline": {"kernel": "decode", "bound": "hbm", "achieved": dec_gbs, "peak": peak,
+                     "peak_source": peak_kind, "unit": "GB/s", "frac": dec_gbs / peak,
+                     "traffic": _traffic_from_profile(f"decode_{cfg.name}")},
+        "roofline_inject": {"kernel": "inject", "bound": "hbm", "achieved": inj_gbs,
+                            "peak": peak, "unit": "GB/s", "frac": inj_gbs / peak,
+                            "traffic": _traffic_from_profile(f"inject_{cfg.name}")},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--variant", type=int, default=0, help="decode kernel: 0 auto, 1 FMA, 2 mma")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

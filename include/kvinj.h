@@ -1,0 +1,210 @@
+/*
+ * kvinj.h -- C ABI of the GB300 (sm_103a) paged KV-injection library.
+ *
+ * The hot path of InferScale-style KV injection and of paged GQA decode:
+ *
+ *   kvinj_slot_mapping  position -> physical slot through a block table
+ *   kvinj_inject        gather pre-RoPE chunk K/V from a resident chunk pool,
+ *                       rotate K at each chunk's assigned absolute position,
+ *                       scatter K/V into a request's paged blocks
+ *   kvinj_append        write one step's new K (rotated) / V at their slots
+ *   kvinj_paged_decode  softmax(q K^T * scale) V of one query per request over
+ *                       the request's non-contiguous blocks (split-K over the
+ *                       context, online softmax, in-kernel combine)
+ *
+ * Sources (web pages, by title and section):
+ *   "InferScale: GPU-Native KV Injection for Personalized LLM Serving":
+ *     §2.3 RoPE, R_a^T R_b = R_{b-a}; §3.1 keys stored before RoPE;
+ *     §3.3 composition applies RoPE to stored keys at the assigned positions;
+ *     §3.4 the worker scatter-copies the composed KV into the allocated paged
+ *     blocks via the slot mapping; per-fact size 2*L*c*h*d*b; §5.1 Theorem 1.
+ *   "LLM Inference: KV Caching": "First, what K and V are" (attention),
+ *     "The fix" (append), "What the cache costs", "Paged attention".
+ *   "Inside LLM Inference Engines: KV Caching, PagedAttention, and Continuous
+ *     Batching": "PagedAttention: Virtual Memory for LLM Generation".
+ *   "Latency Optimization > KV Cache Management": 16-token pages read through
+ *     a page table by the attention kernel.
+ *
+ * Conventions (all entry points):
+ *   - Every array pointer is a DEVICE pointer owned by the caller, except the
+ *     output of kvinj_rope_table_host (host memory). The library allocates and
+ *     frees nothing, keeps no global state, and never synchronises: each call
+ *     enqueues its kernels on `stream` (NULL = legacy default stream) and
+ *     returns. Results are visible to later work on the same stream.
+ *   - Return value: KVINJ_OK, or an error code for arguments the host can see
+ *     are wrong (nothing is launched then), or KVINJ_ECUDA when a launch fails.
+ *   - Bad indices that only the device sees (chunk id, slot, block-table
+ *     entry, position, context length) never trap: the element is skipped (a
+ *     decode page with a bad block is treated as masked) and a KVINJ_ST_* bit
+ *     is OR-ed into *dev_status (a caller-owned device int32; may be NULL).
+ *   - Element types: 16-bit floats (bf16 or fp16), the same type for pool,
+ *     cache, queries and outputs. Pointers to 16-bit data must be 16-byte
+ *     aligned.
+ *   - Layouts (row-major, innermost last):
+ *       pool   [num_chunks][L][2 (K, V)][chunk_len][Hkv][D]   keys pre-RoPE
+ *       cache  k, v: [L][num_blocks][Hkv][block_size][D]       keys post-RoPE
+ *              (one (block, head) page of block_size*D elements is contiguous)
+ *       rope table (device) float4 [max_pos][D/2]
+ *              {cos_hi, sin_hi, cos_lo, sin_lo}: cos/sin of pos*theta^(-2i/D)
+ *              evaluated in fp64 and split into two fp32 parts (hi + lo).
+ *   - RoPE is rotate-half: pair (x_i, x_{i+D/2}) turns by pos*theta^(-2i/D).
+ */
+#ifndef KVINJ_H
+#define KVINJ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *kvinj_stream_t; /* a cudaStream_t */
+
+/* element types */
+#define KVINJ_BF16 0
+#define KVINJ_FP16 1
+
+/* return codes */
+#define KVINJ_OK 0
+#define KVINJ_EINVAL 1       /* null/misaligned pointer, inconsistent shapes */
+#define KVINJ_EUNSUPPORTED 2 /* a shape this build has no kernel for */
+#define KVINJ_EWORKSPACE 3   /* decode workspace too small */
+#define KVINJ_ECUDA 4        /* a CUDA launch or driver call failed */
+
+/* device status bits, OR-ed into *dev_status */
+#define KVINJ_ST_BAD_CHUNK 0x01 /* chunk id outside [0, num_chunks)            */
+#define KVINJ_ST_BAD_SLOT 0x02  /* slot outside [0, num_blocks*block_size)     */
+#define KVINJ_ST_BAD_BLOCK 0x04 /* block-table entry outside [0, num_blocks)   */
+#define KVINJ_ST_BAD_POS 0x08   /* position < 0, beyond the table or the rope table */
+#define KVINJ_ST_BAD_CTX 0x10   /* context length <= 0 or > max_blocks*block_size */
+#define KVINJ_ST_BAD_SEQ 0x20   /* sequence id outside [0, batch)              */
+#define KVINJ_ST_TIMEOUT 0x40   /* a pipeline wait gave up (kernel returned early) */
+
+/* paged KV cache of one model (all layers) */
+typedef struct {
+  int32_t num_layers;   /* L */
+  int32_t num_kv_heads; /* Hkv */
+  int32_t head_dim;     /* D: 64 or 128 (inject/append also 256) */
+  int32_t block_size;   /* tokens per block (decode: 16) */
+  int64_t num_blocks;   /* physical blocks per layer */
+  int32_t dtype;        /* KVINJ_BF16 / KVINJ_FP16 */
+  void *k;              /* device [L][num_blocks][Hkv][block_size][D] */
+  void *v;              /* device, same layout */
+} kvinj_cache;
+
+/* resident pool of pre-RoPE memory chunks ("facts"), one contiguous record
+ * of 2*L*chunk_len*Hkv*D elements per chunk (InferScale §3.4) */
+typedef struct {
+  int32_t num_layers, num_kv_heads, head_dim;
+  int32_t chunk_len;  /* c: tokens per chunk */
+  int64_t num_chunks; /* records in the pool */
+  int32_t dtype;
+  const void *data; /* device [num_chunks][L][2][c][Hkv][D] */
+} kvinj_pool;
+
+/* RoPE table on the device (layout in the header comment) */
+typedef struct {
+  const void *table; /* device float4 [max_pos][head_dim/2] */
+  int32_t max_pos;   /* positions 0 .. max_pos-1 are valid */
+  int32_t head_dim;
+} kvinj_rope;
+
+/* Bytes of the RoPE table for (head_dim, max_pos): max_pos*head_dim/2*16. */
+size_t kvinj_rope_table_bytes(int32_t head_dim, int32_t max_pos);
+
+/* Fill a HOST buffer of kvinj_rope_table_bytes() bytes: entry [p][i] holds
+ * cos and sin of p * theta^(-2i/head_dim), computed in fp64, each split into
+ * hi = (float)x and lo = (float)(x - hi). The caller copies it to the device.
+ * InferScale §2.3 (R_p) and §3.3 (RoPE applied with the rotary tables).
+ * Returns KVINJ_EINVAL for head_dim odd or <= 0, max_pos <= 0, theta <= 0,
+ * out == NULL. */
+int kvinj_rope_table_host(double theta, int32_t head_dim, int32_t max_pos, float *out);
+
+/* Slot mapping (InferScale §3.4; "LLM Inference: KV Caching", Paged
+ * attention): slot_out[i] = block_tables[seq_ids[i]][positions[i] / B] * B
+ * + positions[i] % B, as int64. block_tables [batch][max_blocks] int32.
+ * Invalid sequence id, position or block entry: slot_out[i] = -1 and the
+ * matching KVINJ_ST_* bit. n == 0 is a no-op. */
+int kvinj_slot_mapping(const int32_t *block_tables, int32_t max_blocks, int32_t batch,
+                       int64_t num_blocks, int32_t block_size, const int32_t *seq_ids,
+                       const int32_t *positions, int64_t n, int64_t *slot_out,
+                       int32_t *dev_status, kvinj_stream_t stream);
+
+/* Inject (InferScale §3.3, §3.4, §5.1). For the j-th injected chunk
+ * (j < n_inj) and each layer l in [layer_begin, layer_end): token t < c of
+ * pool record chunk_ids[j] takes absolute position start_pos[j] + t and slot
+ * slot_mapping[j*c + t]; its K row of each kv head is rotated there (fp32
+ * arithmetic with the fp64-derived table, rounded once, nearest-even) and
+ * written to k[l][slot / B][h][slot % B][:], its V row is copied bit for bit
+ * to v. Pool and cache must agree in L, Hkv, D and dtype; rope->head_dim ==
+ * D. Chunks that overlap in slots race (undefined which one wins). */
+int kvinj_inject(const kvinj_pool *pool, const kvinj_cache *cache, const kvinj_rope *rope,
+                 const int32_t *chunk_ids, const int32_t *start_pos,
+                 const int64_t *slot_mapping, int32_t n_inj, int32_t layer_begin,
+                 int32_t layer_end, int32_t *dev_status, kvinj_stream_t stream);
+
+/* Append ("LLM Inference: KV Caching", The fix): token i < n writes
+ * k_new[i][h][:] rotated at positions[i] (copied as given when rope == NULL)
+ * and v_new[i][h][:] to layer `layer` at slot_mapping[i].
+ * k_new, v_new: device [n][Hkv][D] in the cache dtype. */
+int kvinj_append(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                 const void *k_new, const void *v_new, const int32_t *positions,
+                 const int64_t *slot_mapping, int64_t n, int32_t *dev_status,
+                 kvinj_stream_t stream);
+
+/* Workspace bytes kvinj_paged_decode needs for this shape on the current
+ * device (partial softmax states of the split-K pieces plus one counter per
+ * (request, kv head)). */
+size_t kvinj_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim);
+
+/* Zero a decode workspace (its counters must start at zero; every decode call
+ * leaves them at zero again). Call once after allocating it. */
+int kvinj_decode_workspace_init(void *workspace, size_t ws_bytes, kvinj_stream_t stream);
+
+/* Paged decode attention ("LLM Inference: KV Caching", attention and Paged
+ * attention; "Latency Optimization > KV Cache Management"). For request r <
+ * batch and query head qh < Hq (kv head h = qh / (Hq/Hkv), consecutive
+ * groups), with C = context_lens[r] tokens at positions 0..C-1 read from
+ * k/v[layer][block_tables[r][p / 16]][h][p % 16]:
+ *   q' = R_{q_pos[r]} q[r][qh]   (q taken as given when rope == NULL)
+ *   out[r][qh] = sum_p softmax_p(scale * q'.K_p) V_p
+ * scale <= 0 means 1/sqrt(D). q, out: device [batch][Hq][D] in the cache
+ * dtype; accumulation is fp32. workspace: device, at least
+ * kvinj_decode_workspace_size() bytes, zeroed once by
+ * kvinj_decode_workspace_init(); calls sharing one workspace must not overlap
+ * in time. A request with an invalid context gets a zero output and
+ * KVINJ_ST_BAD_CTX. Requires block_size 16, D 64 or 128, Hq % Hkv == 0,
+ * Hq/Hkv <= 16 and batch <= 4096 (KVINJ_EUNSUPPORTED otherwise). */
+int kvinj_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                       int32_t num_q_heads, const void *q, const int32_t *q_pos,
+                       const int32_t *block_tables, int32_t max_blocks,
+                       const int32_t *context_lens, int32_t batch, float scale, void *out,
+                       void *workspace, size_t ws_bytes, int32_t *dev_status,
+                       kvinj_stream_t stream);
+
+/* Same as kvinj_paged_decode with an explicit kernel choice:
+ * variant 0 = automatic, 1 = CUDA-core FMA kernel, 2 = tensor-core (mma)
+ * kernel. `ctas` > 0 overrides the grid size (1 .. number of workspace
+ * slots); 0 = one CTA per SM. */
+int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                          int32_t num_q_heads, const void *q, const int32_t *q_pos,
+                          const int32_t *block_tables, int32_t max_blocks,
+                          const int32_t *context_lens, int32_t batch, float scale, void *out,
+                          void *workspace, size_t ws_bytes, int32_t *dev_status,
+                          kvinj_stream_t stream, int32_t variant, int32_t ctas);
+
+/* KV bytes of `tokens` tokens: 2 * layers * heads * head_dim * tokens *
+ * bytes_per_elem ("LLM Inference: KV Caching", What the cache costs). */
+int64_t kvinj_kv_bytes(int32_t layers, int32_t heads, int32_t head_dim, int64_t tokens,
+                       int32_t bytes_per_elem);
+
+/* Static description of a return code. */
+const char *kvinj_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVINJ_H */

@@ -1,0 +1,322 @@
+// kvinj_api.cu -- the extern "C" entry points declared in include/kvinj.h:
+// argument validation, the fp64 RoPE table, TMA tensor maps and dispatch to
+// the kernels. Host code only.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "kvinj.h"
+#include "kvinj_internal.h"
+
+namespace kvinj {
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
+size_t decode_partial_floats(int G, int D) { return (size_t)G * (size_t)(D + 2); }
+int decode_max_ctas() { return 4 * num_sms(); }
+size_t decode_counters_bytes(int batch, int Hkv) {
+  return (((size_t)batch * Hkv * sizeof(int)) + 255) & ~size_t(255);
+}
+
+}  // namespace kvinj
+
+using namespace kvinj;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+bool dtype_ok(int dt) { return dt == KVINJ_BF16 || dt == KVINJ_FP16; }
+
+int check_cache(const kvinj_cache *c, bool decode) {
+  if (!c || !c->k || !c->v) return KVINJ_EINVAL;
+  if (!aligned16(c->k) || !aligned16(c->v)) return KVINJ_EINVAL;
+  if (c->num_layers <= 0 || c->num_kv_heads <= 0 || c->num_blocks <= 0 || c->block_size <= 0)
+    return KVINJ_EINVAL;
+  if (!dtype_ok(c->dtype)) return KVINJ_EINVAL;
+  if (decode) {
+    if (c->head_dim != 64 && c->head_dim != 128) return KVINJ_EUNSUPPORTED;
+    if (c->block_size != 16) return KVINJ_EUNSUPPORTED;
+  } else if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) {
+    return KVINJ_EUNSUPPORTED;
+  }
+  return KVINJ_OK;
+}
+
+int check_rope(const kvinj_rope *r, int D) {
+  if (!r) return KVINJ_OK;
+  if (!r->table || r->max_pos <= 0 || r->head_dim != D) return KVINJ_EINVAL;
+  if (!aligned16(r->table)) return KVINJ_EINVAL;
+  return KVINJ_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D view of one cache array: rows of D elements, L*num_blocks*Hkv*16 rows;
+// box 16 rows x 64 elements (128 bytes), 128-byte swizzle
+int make_cache_map(CUtensorMap *m, void *base, const kvinj_cache *c) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return KVINJ_ECUDA;
+  const uint64_t rows = (uint64_t)c->num_layers * (uint64_t)c->num_blocks *
+                        (uint64_t)c->num_kv_heads * (uint64_t)c->block_size;
+  cuuint64_t dims[2] = {(cuuint64_t)c->head_dim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)c->head_dim * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)c->block_size};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KVINJ_OK : KVINJ_ECUDA;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? KVINJ_OK : KVINJ_ECUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t kvinj_rope_table_bytes(int32_t head_dim, int32_t max_pos) {
+  if (head_dim <= 0 || max_pos <= 0) return 0;
+  return (size_t)max_pos * (size_t)(head_dim / 2) * 4 * sizeof(float);
+}
+
+int kvinj_rope_table_host(double theta, int32_t head_dim, int32_t max_pos, float *out) {
+  if (!out || head_dim <= 0 || (head_dim & 1) || max_pos <= 0 || !(theta > 0.0))
+    return KVINJ_EINVAL;
+  const int half = head_dim / 2;
+  for (int i = 0; i < half; ++i) {
+    const double inv_freq = pow(theta, -(double)(2 * i) / (double)head_dim);
+    for (int64_t p = 0; p < max_pos; ++p) {
+      const double ang = (double)p * inv_freq;
+      const double c = cos(ang), s = sin(ang);
+      const float ch = (float)c, sh = (float)s;
+      float *e = out + ((size_t)p * half + i) * 4;
+      e[0] = ch;
+      e[1] = sh;
+      e[2] = (float)(c - (double)ch);
+      e[3] = (float)(s - (double)sh);
+    }
+  }
+  return KVINJ_OK;
+}
+
+int kvinj_slot_mapping(const int32_t *block_tables, int32_t max_blocks, int32_t batch,
+                       int64_t num_blocks, int32_t block_size, const int32_t *seq_ids,
+                       const int32_t *positions, int64_t n, int64_t *slot_out,
+                       int32_t *dev_status, kvinj_stream_t stream) {
+  if (n < 0) return KVINJ_EINVAL;
+  if (n == 0) return KVINJ_OK;
+  if (!block_tables || !seq_ids || !positions || !slot_out) return KVINJ_EINVAL;
+  if (max_blocks <= 0 || batch <= 0 || num_blocks <= 0 || block_size <= 0) return KVINJ_EINVAL;
+  return cuda_rc(launch_slot_mapping(block_tables, max_blocks, batch, num_blocks, block_size,
+                                     seq_ids, positions, n, slot_out, dev_status,
+                                     (cudaStream_t)stream));
+}
+
+int kvinj_inject(const kvinj_pool *pool, const kvinj_cache *cache, const kvinj_rope *rope,
+                 const int32_t *chunk_ids, const int32_t *start_pos,
+                 const int64_t *slot_mapping, int32_t n_inj, int32_t layer_begin,
+                 int32_t layer_end, int32_t *dev_status, kvinj_stream_t stream) {
+  int rc = check_cache(cache, false);
+  if (rc) return rc;
+  if (!pool || !pool->data || !aligned16(pool->data)) return KVINJ_EINVAL;
+  if (pool->num_layers != cache->num_layers || pool->num_kv_heads != cache->num_kv_heads ||
+      pool->head_dim != cache->head_dim || pool->dtype != cache->dtype ||
+      pool->chunk_len <= 0 || pool->num_chunks <= 0)
+    return KVINJ_EINVAL;
+  if (!rope) return KVINJ_EINVAL;
+  if ((rc = check_rope(rope, cache->head_dim))) return rc;
+  if (n_inj < 0 || layer_begin < 0 || layer_end > cache->num_layers || layer_begin > layer_end)
+    return KVINJ_EINVAL;
+  if (n_inj == 0 || layer_begin == layer_end) return KVINJ_OK;
+  if (!chunk_ids || !start_pos || !slot_mapping) return KVINJ_EINVAL;
+  InjectArgs a;
+  a.pool = static_cast<const uint16_t *>(pool->data);
+  a.L = cache->num_layers;
+  a.Hkv = cache->num_kv_heads;
+  a.chunk_len = pool->chunk_len;
+  a.num_chunks = pool->num_chunks;
+  a.k = static_cast<uint16_t *>(cache->k);
+  a.v = static_cast<uint16_t *>(cache->v);
+  a.num_blocks = cache->num_blocks;
+  a.B = cache->block_size;
+  a.rope = static_cast<const float4 *>(rope->table);
+  a.max_pos = rope->max_pos;
+  a.chunk_ids = chunk_ids;
+  a.start_pos = start_pos;
+  a.slot_mapping = slot_mapping;
+  a.n_inj = n_inj;
+  a.layer_begin = layer_begin;
+  a.n_layers = layer_end - layer_begin;
+  a.status = dev_status;
+  return cuda_rc(launch_inject(a, cache->head_dim, cache->dtype, (cudaStream_t)stream));
+}
+
+int kvinj_append(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                 const void *k_new, const void *v_new, const int32_t *positions,
+                 const int64_t *slot_mapping, int64_t n, int32_t *dev_status,
+                 kvinj_stream_t stream) {
+  int rc = check_cache(cache, false);
+  if (rc) return rc;
+  if ((rc = check_rope(rope, cache->head_dim))) return rc;
+  if (n < 0 || layer < 0 || layer >= cache->num_layers) return KVINJ_EINVAL;
+  if (n == 0) return KVINJ_OK;
+  if (!k_new || !v_new || !positions || !slot_mapping) return KVINJ_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new)) return KVINJ_EINVAL;
+  AppendArgs a;
+  a.k = static_cast<uint16_t *>(cache->k);
+  a.v = static_cast<uint16_t *>(cache->v);
+  a.Hkv = cache->num_kv_heads;
+  a.num_blocks = cache->num_blocks;
+  a.B = cache->block_size;
+  a.layer = layer;
+  a.k_new = static_cast<const uint16_t *>(k_new);
+  a.v_new = static_cast<const uint16_t *>(v_new);
+  a.positions = positions;
+  a.slot_mapping = slot_mapping;
+  a.n = n;
+  a.rope = rope ? static_cast<const float4 *>(rope->table) : nullptr;
+  a.max_pos = rope ? rope->max_pos : 0;
+  a.status = dev_status;
+  return cuda_rc(launch_append(a, cache->head_dim, cache->dtype, (cudaStream_t)stream));
+}
+
+size_t kvinj_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim) {
+  if (batch <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads ||
+      head_dim <= 0)
+    return 0;
+  const int G = num_q_heads / num_kv_heads;
+  return decode_counters_bytes(batch, num_kv_heads) +
+         (size_t)2 * decode_max_ctas() * decode_partial_floats(G, head_dim) * sizeof(float);
+}
+
+int kvinj_decode_workspace_init(void *workspace, size_t ws_bytes, kvinj_stream_t stream) {
+  if (!workspace && ws_bytes) return KVINJ_EINVAL;
+  if (!ws_bytes) return KVINJ_OK;
+  return cuda_rc(cudaMemsetAsync(workspace, 0, ws_bytes, (cudaStream_t)stream));
+}
+
+int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                          int32_t num_q_heads, const void *q, const int32_t *q_pos,
+                          const int32_t *block_tables, int32_t max_blocks,
+                          const int32_t *context_lens, int32_t batch, float scale, void *out,
+                          void *workspace, size_t ws_bytes, int32_t *dev_status,
+                          kvinj_stream_t stream, int32_t variant, int32_t ctas) {
+  int rc = check_cache(cache, true);
+  if (rc) return rc;
+  const int D = cache->head_dim, Hkv = cache->num_kv_heads;
+  if ((rc = check_rope(rope, D))) return rc;
+  if (layer < 0 || layer >= cache->num_layers || batch < 0 || max_blocks <= 0) return KVINJ_EINVAL;
+  if (num_q_heads <= 0 || num_q_heads % Hkv) return KVINJ_EINVAL;
+  const int G = num_q_heads / Hkv;
+  if (batch == 0) return KVINJ_OK;
+  if (!q || !block_tables || !context_lens || !out || !workspace) return KVINJ_EINVAL;
+  if (rope && !q_pos) return KVINJ_EINVAL;
+  if (!aligned16(q) || !aligned16(out)) return KVINJ_EINVAL;
+  if (variant < 0 || variant > 2) return KVINJ_EINVAL;
+  if (variant == 0) variant = 1;
+  if (variant == 1 && !(G == 1 || G == 2 || G == 4 || G == 8)) return KVINJ_EUNSUPPORTED;
+  if (variant == 2) return KVINJ_EUNSUPPORTED;
+  if ((int64_t)batch * Hkv * max_blocks >= (int64_t)1 << 31) return KVINJ_EUNSUPPORTED;
+  if (batch > 4096) return KVINJ_EUNSUPPORTED;  // per-request prefix sums live in shared memory
+  if ((int64_t)cache->num_layers * cache->num_blocks * Hkv * 16 >= (int64_t)1 << 31)
+    return KVINJ_EUNSUPPORTED;
+  if (ws_bytes < kvinj_decode_workspace_size(batch, num_q_heads, Hkv, D)) return KVINJ_EWORKSPACE;
+  const int max_ctas = decode_max_ctas();
+  if (ctas < 0 || ctas > max_ctas) return KVINJ_EINVAL;
+  if (ctas == 0) ctas = num_sms();
+
+  CUtensorMap tmK, tmV;
+  if ((rc = make_cache_map(&tmK, cache->k, cache))) return rc;
+  if ((rc = make_cache_map(&tmV, cache->v, cache))) return rc;
+
+  DecodeArgs a;
+  a.q = static_cast<const uint16_t *>(q);
+  a.q_pos = q_pos;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.rope = rope ? static_cast<const float4 *>(rope->table) : nullptr;
+  a.max_pos = rope ? rope->max_pos : 0;
+  a.out = static_cast<uint16_t *>(out);
+  a.counters = static_cast<int *>(workspace);
+  a.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                         decode_counters_bytes(batch, Hkv));
+  a.status = dev_status;
+  a.batch = batch;
+  a.Hq = num_q_heads;
+  a.Hkv = Hkv;
+  a.max_blocks = max_blocks;
+  a.layer = layer;
+  a.num_blocks = cache->num_blocks;
+  const double sc = scale > 0.f ? (double)scale : 1.0 / sqrt((double)D);
+  a.scale_log2 = (float)(sc * 1.4426950408889634);
+  return cuda_rc(launch_decode(a, tmK, tmV, D, G, cache->dtype, variant, ctas,
+                               (cudaStream_t)stream));
+}
+
+int kvinj_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                       int32_t num_q_heads, const void *q, const int32_t *q_pos,
+                       const int32_t *block_tables, int32_t max_blocks,
+                       const int32_t *context_lens, int32_t batch, float scale, void *out,
+                       void *workspace, size_t ws_bytes, int32_t *dev_status,
+                       kvinj_stream_t stream) {
+  return kvinj_paged_decode_ex(cache, rope, layer, num_q_heads, q, q_pos, block_tables,
+                               max_blocks, context_lens, batch, scale, out, workspace, ws_bytes,
+                               dev_status, stream, 0, 0);
+}
+
+int64_t kvinj_kv_bytes(int32_t layers, int32_t heads, int32_t head_dim, int64_t tokens,
+                       int32_t bytes_per_elem) {
+  return (int64_t)2 * layers * heads * head_dim * tokens * bytes_per_elem;
+}
+
+const char *kvinj_strerror(int code) {
+  switch (code) {
+    case KVINJ_OK: return "ok";
+    case KVINJ_EINVAL: return "invalid argument (null or misaligned pointer, inconsistent shape)";
+    case KVINJ_EUNSUPPORTED: return "unsupported shape for this build";
+    case KVINJ_EWORKSPACE: return "decode workspace too small";
+    case KVINJ_ECUDA: return "CUDA launch or driver call failed";
+  }
+  return "unknown error code";
+}
+
+}  // extern "C"
+
+namespace kvinj {
+cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                          int D, int G, int dtype, int variant, int ctas, cudaStream_t s) {
+  if (variant == 1) return launch_decode_ffma(a, tmK, tmV, D, G, dtype, ctas, s);
+  return cudaErrorInvalidValue;
+}
+}  // namespace kvinj

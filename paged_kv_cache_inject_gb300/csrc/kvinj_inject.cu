@@ -1,0 +1,267 @@
+// kvinj_inject.cu -- slot mapping, inject (gather pre-RoPE chunk rows, rotate
+// K at the assigned absolute position, scatter into paged blocks) and append.
+//
+// "InferScale: GPU-Native KV Injection for Personalized LLM Serving" §3.3
+// (compose retrieved pre-RoPE facts, RoPE applied at the assigned positions)
+// and §3.4 (the worker scatter-copies the composed KV into the allocated
+// blocks via the slot mapping, a same-device copy); §5.1 Theorem 1 (the
+// relocation is exact, so rotating stored keys at injection time is valid).
+// "LLM Inference: KV Caching", "The fix": each decode step appends one
+// token's K/V per layer; "Paged attention": block table -> physical blocks.
+//
+// Design (GB300): the path is a gather-rotate-scatter of 2*D-byte rows, bound
+// by HBM bandwidth. A warp takes one unit = (chunk, layer, token): all Hkv K
+// rows and all Hkv V rows of that token. Each 16-lane half-warp handles one
+// row; lane k owns elements [E*k, E*k+E) of the first half of the row and the
+// same offsets of the second half (E = D/32), so the rotate-half partner of
+// every element sits in the same lane: no shuffles, and every load/store
+// instruction of the warp covers two full 128-byte lines (D = 128). All loads
+// of a unit are issued before its stores (4 row pairs per batch) to keep
+// enough bytes in flight. The cos/sin table row of the token's position is
+// loaded once per unit and reused for its Hkv rows. The grid is persistent
+// (a multiple of the SM count) and walks the units in pool order, so reads
+// stream through each chunk's contiguous K (then V) block.
+#include "kvinj_device.cuh"
+#include "kvinj_internal.h"
+
+namespace kvinj {
+
+// ---------------------------------------------------------------------------
+// slot mapping
+// ---------------------------------------------------------------------------
+__global__ void slot_mapping_kernel(const int32_t *__restrict__ bt, int max_blocks, int batch,
+                                    int64_t num_blocks, int B, const int32_t *__restrict__ seq,
+                                    const int32_t *__restrict__ pos, int64_t n,
+                                    int64_t *__restrict__ out, int32_t *status) {
+  int bad = 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    int r = seq[i], p = pos[i];
+    int64_t slot = -1;
+    if (r < 0 || r >= batch) {
+      bad |= KVINJ_ST_BAD_SEQ;
+    } else if (p < 0 || p / B >= max_blocks) {
+      bad |= KVINJ_ST_BAD_POS;
+    } else {
+      int blk = bt[(int64_t)r * max_blocks + p / B];
+      if (blk < 0 || blk >= num_blocks)
+        bad |= KVINJ_ST_BAD_BLOCK;
+      else
+        slot = (int64_t)blk * B + p % B;
+    }
+    out[i] = slot;
+  }
+  if (bad) report(status, bad);
+}
+
+// ---------------------------------------------------------------------------
+// row rotation + copy for one unit
+// ---------------------------------------------------------------------------
+template <int D>
+struct RowVec {
+  static constexpr int E = D / 32;  // elements per lane per half row
+  static constexpr int W = E / 2;   // 32-bit words per lane per half row
+  using T = typename Vec<E * 2>::T;
+};
+
+template <int W>
+struct Words {
+  uint32_t w[W];
+};
+
+template <int D>
+__device__ __forceinline__ Words<RowVec<D>::W> load_half(const uint16_t *p) {
+  using T = typename RowVec<D>::T;
+  T v = ld_stream(reinterpret_cast<const T *>(p));
+  Words<RowVec<D>::W> r;
+  static_assert(sizeof(T) == sizeof(r), "vector width");
+  memcpy(&r, &v, sizeof(T));
+  return r;
+}
+
+template <int D>
+__device__ __forceinline__ void store_half(uint16_t *p, const Words<RowVec<D>::W> &r) {
+  using T = typename RowVec<D>::T;
+  T v;
+  memcpy(&v, &r, sizeof(T));
+  st_global(reinterpret_cast<T *>(p), v);
+}
+
+// Process the Hkv K rows (rotated with `rot` = table row of the position, or
+// copied when rot == nullptr) and Hkv V rows (copied) of one token.
+// Source row of head h: sk + h*s_stride; destination: dk + h*d_stride.
+template <int D, int DT>
+__device__ __forceinline__ void process_token(const uint16_t *sk, const uint16_t *sv,
+                                              int64_t s_stride, uint16_t *dk, uint16_t *dv,
+                                              int64_t d_stride, int Hkv, const float4 *rot,
+                                              int lane) {
+  constexpr int E = RowVec<D>::E, W = RowVec<D>::W, HALF = D / 2, RB = 4;
+  const int half = lane >> 4, k = lane & 15;
+  float4 tab[E];
+  if (rot) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) tab[e] = __ldg(rot + k * E + e);
+  }
+  for (int h0 = 0; h0 < Hkv; h0 += 2 * RB) {
+    Words<W> klo[RB], khi[RB], vlo[RB], vhi[RB];
+#pragma unroll
+    for (int i = 0; i < RB; ++i) {
+      int h = h0 + 2 * i + half;
+      if (h < Hkv) {
+        const uint16_t *ks = sk + h * s_stride + k * E;
+        const uint16_t *vs = sv + h * s_stride + k * E;
+        klo[i] = load_half<D>(ks);
+        khi[i] = load_half<D>(ks + HALF);
+        vlo[i] = load_half<D>(vs);
+        vhi[i] = load_half<D>(vs + HALF);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < RB; ++i) {
+      int h = h0 + 2 * i + half;
+      if (h < Hkv) {
+        if (rot) {
+#pragma unroll
+          for (int w = 0; w < W; ++w) {
+            float2 a = unpack2<DT>(klo[i].w[w]);
+            float2 b = unpack2<DT>(khi[i].w[w]);
+            float2 y0 = rope_pair(a.x, b.x, tab[2 * w]);
+            float2 y1 = rope_pair(a.y, b.y, tab[2 * w + 1]);
+            klo[i].w[w] = pack2<DT>(y0.x, y1.x);
+            khi[i].w[w] = pack2<DT>(y0.y, y1.y);
+          }
+        }
+        uint16_t *kd = dk + h * d_stride + k * E;
+        uint16_t *vd = dv + h * d_stride + k * E;
+        store_half<D>(kd, klo[i]);
+        store_half<D>(kd + HALF, khi[i]);
+        store_half<D>(vd, vlo[i]);
+        store_half<D>(vd + HALF, vhi[i]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// inject
+// ---------------------------------------------------------------------------
+template <int D, int DT>
+__global__ void __launch_bounds__(256) inject_kernel(InjectArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t c = a.chunk_len;
+  const int64_t n_units = (int64_t)a.n_inj * a.n_layers * c;
+  const int64_t row = (int64_t)a.Hkv * D;
+  const int64_t nslots = a.num_blocks * a.B;
+  for (int64_t u = warp; u < n_units; u += nwarps) {
+    const int t = (int)(u % c);
+    const int64_t jl = u / c;
+    const int l = a.layer_begin + (int)(jl % a.n_layers);
+    const int j = (int)(jl / a.n_layers);
+    const int id = a.chunk_ids[j];
+    const int64_t slot = a.slot_mapping[(int64_t)j * c + t];
+    const int pos = a.start_pos[j] + t;
+    int bad = 0;
+    if (id < 0 || id >= a.num_chunks) bad |= KVINJ_ST_BAD_CHUNK;
+    if (slot < 0 || slot >= nslots) bad |= KVINJ_ST_BAD_SLOT;
+    if (pos < 0 || pos >= a.max_pos) bad |= KVINJ_ST_BAD_POS;
+    if (bad) {
+      if (lane == 0) report(a.status, bad);
+      continue;
+    }
+    const uint16_t *sk = a.pool + (((int64_t)id * a.L + l) * 2 * c + t) * row;
+    const uint16_t *sv = sk + c * row;
+    const int64_t dst = (((int64_t)l * a.num_blocks + slot / a.B) * a.Hkv * a.B + slot % a.B) * D;
+    process_token<D, DT>(sk, sv, D, a.k + dst, a.v + dst, (int64_t)a.B * D, a.Hkv,
+                         a.rope + (int64_t)pos * (D / 2), lane);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// append
+// ---------------------------------------------------------------------------
+template <int D, int DT>
+__global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t row = (int64_t)a.Hkv * D;
+  const int64_t nslots = a.num_blocks * a.B;
+  for (int64_t i = warp; i < a.n; i += nwarps) {
+    const int64_t slot = a.slot_mapping[i];
+    const int pos = a.positions[i];
+    int bad = 0;
+    if (slot < 0 || slot >= nslots) bad |= KVINJ_ST_BAD_SLOT;
+    if (pos < 0 || (a.rope && pos >= a.max_pos)) bad |= KVINJ_ST_BAD_POS;
+    if (bad) {
+      if (lane == 0) report(a.status, bad);
+      continue;
+    }
+    const int64_t dst =
+        (((int64_t)a.layer * a.num_blocks + slot / a.B) * a.Hkv * a.B + slot % a.B) * D;
+    process_token<D, DT>(a.k_new + i * row, a.v_new + i * row, D, a.k + dst, a.v + dst,
+                         (int64_t)a.B * D, a.Hkv,
+                         a.rope ? a.rope + (int64_t)pos * (D / 2) : nullptr, lane);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+static int persistent_grid(int64_t warps_of_work) {
+  int64_t ctas = (warps_of_work + 7) / 8;
+  int64_t cap = (int64_t)num_sms() * 8;
+  if (ctas > cap) ctas = cap;
+  return (int)(ctas < 1 ? 1 : ctas);
+}
+
+cudaError_t launch_slot_mapping(const int32_t *bt, int max_blocks, int batch, int64_t num_blocks,
+                                int B, const int32_t *seq, const int32_t *pos, int64_t n,
+                                int64_t *out, int32_t *status, cudaStream_t s) {
+  int64_t ctas = (n + 255) / 256;
+  int64_t cap = (int64_t)num_sms() * 8;
+  if (ctas > cap) ctas = cap;
+  slot_mapping_kernel<<<(int)ctas, 256, 0, s>>>(bt, max_blocks, batch, num_blocks, B, seq, pos,
+                                                n, out, status);
+  return cudaGetLastError();
+}
+
+template <int D, int DT>
+static cudaError_t inject_dt(const InjectArgs &a, cudaStream_t s) {
+  int64_t units = (int64_t)a.n_inj * a.n_layers * a.chunk_len;
+  inject_kernel<D, DT><<<persistent_grid(units), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_inject(const InjectArgs &a, int D, int dtype, cudaStream_t s) {
+  switch (D * 2 + dtype) {
+    case 64 * 2 + 0: return inject_dt<64, 0>(a, s);
+    case 64 * 2 + 1: return inject_dt<64, 1>(a, s);
+    case 128 * 2 + 0: return inject_dt<128, 0>(a, s);
+    case 128 * 2 + 1: return inject_dt<128, 1>(a, s);
+    case 256 * 2 + 0: return inject_dt<256, 0>(a, s);
+    case 256 * 2 + 1: return inject_dt<256, 1>(a, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <int D, int DT>
+static cudaError_t append_dt(const AppendArgs &a, cudaStream_t s) {
+  append_kernel<D, DT><<<persistent_grid(a.n), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const AppendArgs &a, int D, int dtype, cudaStream_t s) {
+  switch (D * 2 + dtype) {
+    case 64 * 2 + 0: return append_dt<64, 0>(a, s);
+    case 64 * 2 + 1: return append_dt<64, 1>(a, s);
+    case 128 * 2 + 0: return append_dt<128, 0>(a, s);
+    case 128 * 2 + 1: return append_dt<128, 1>(a, s);
+    case 256 * 2 + 0: return append_dt<256, 0>(a, s);
+    case 256 * 2 + 1: return append_dt<256, 1>(a, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvinj

@@ -1,0 +1,76 @@
+// kvinj_internal.h -- declarations shared by the library's translation units
+// (kernel argument blocks and launchers). Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kvinj {
+
+int num_sms();  // SMs of the current device (cached per device)
+
+struct InjectArgs {
+  const uint16_t *pool;
+  int L, Hkv, chunk_len;
+  int64_t num_chunks;
+  uint16_t *k, *v;
+  int64_t num_blocks;
+  int B;
+  const float4 *rope;
+  int max_pos;
+  const int32_t *chunk_ids, *start_pos;
+  const int64_t *slot_mapping;
+  int n_inj, layer_begin, n_layers;
+  int32_t *status;
+};
+
+struct AppendArgs {
+  uint16_t *k, *v;
+  int Hkv;
+  int64_t num_blocks;
+  int B, layer;
+  const uint16_t *k_new, *v_new;
+  const int32_t *positions;
+  const int64_t *slot_mapping;
+  int64_t n;
+  const float4 *rope;  // nullptr: keys already rotated
+  int max_pos;
+  int32_t *status;
+};
+
+struct DecodeArgs {
+  const uint16_t *q;           // [batch][Hq][D]
+  const int32_t *q_pos;        // [batch]
+  const int32_t *block_tables; // [batch][max_blocks]
+  const int32_t *context_lens; // [batch]
+  const float4 *rope;          // nullptr: q already rotated
+  int max_pos;
+  uint16_t *out;               // [batch][Hq][D]
+  float *partials;             // [2*max_ctas][G][D+2]
+  int *counters;               // [batch*Hkv]
+  int32_t *status;
+  int batch, Hq, Hkv, max_blocks, layer;
+  int64_t num_blocks;
+  float scale_log2;            // softmax scale times log2(e)
+};
+
+// decode workspace: counters first, then the partial slots
+size_t decode_partial_floats(int G, int D);  // floats per slot
+int decode_max_ctas();                        // slots/2 the workspace is sized for
+size_t decode_counters_bytes(int batch, int Hkv);
+
+cudaError_t launch_slot_mapping(const int32_t *bt, int max_blocks, int batch, int64_t num_blocks,
+                                int B, const int32_t *seq, const int32_t *pos, int64_t n,
+                                int64_t *out, int32_t *status, cudaStream_t s);
+cudaError_t launch_inject(const InjectArgs &a, int D, int dtype, cudaStream_t s);
+cudaError_t launch_append(const AppendArgs &a, int D, int dtype, cudaStream_t s);
+cudaError_t launch_decode_ffma(const DecodeArgs &a, const CUtensorMap &tmK,
+                               const CUtensorMap &tmV, int D, int G, int dtype, int ctas,
+                               cudaStream_t s);
+// variant: 1 = CUDA-core FMA kernel, 2 = tensor-core kernel
+cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                          int D, int G, int dtype, int variant, int ctas, cudaStream_t s);
+
+}  // namespace kvinj

@@ -1,0 +1,125 @@
+"""A GPU-resident paged KV-injection engine built on the C ABI.
+
+Holds what lives in HBM across requests -- the pre-RoPE chunk pool (the
+store InferScale keeps resident, its §3.1 and §6.7), the paged KV cache of
+all layers, the RoPE table and the decode workspace -- and runs one step of
+the hot path through the library's kernels:
+
+    slot mapping -> inject (all layers) -> per decode step, per layer:
+    append the new token's K/V, paged decode attention
+
+Every operation here is a call into libkvinj.so; this module only sequences
+the calls and owns the buffers. ``step_from_host`` is the end-to-end form a
+caller with host-side request data uses: it copies the step's inputs from
+pinned host memory, runs the step and copies the outputs back.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import kvinj as K
+
+
+@dataclass
+class StepInputs:
+    """Device tensors of one step (one batch of requests)."""
+    chunk_ids: torch.Tensor     # int32 [n_inj]
+    start_pos: torch.Tensor     # int32 [n_inj]
+    map_seq: torch.Tensor       # int32 [n_inj*c + steps*batch]: injected tokens, then step tokens
+    map_pos: torch.Tensor       # int32 [same]
+    block_tables: torch.Tensor  # int32 [batch][max_blocks]
+    ctx_lens: torch.Tensor      # int32 [steps][batch]: context length seen by each decode step
+    q_pos: torch.Tensor         # int32 [steps][batch]: position of each step's new token
+    q: torch.Tensor             # [steps][L][batch][Hq][D]   pre-RoPE queries
+    k_new: torch.Tensor         # [steps][L][batch][Hkv][D]  pre-RoPE keys of the new tokens
+    v_new: torch.Tensor         # [steps][L][batch][Hkv][D]
+
+    def tensors(self):
+        return [self.chunk_ids, self.start_pos, self.map_seq, self.map_pos, self.block_tables,
+                self.ctx_lens, self.q_pos, self.q, self.k_new, self.v_new]
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self.tensors())
+
+
+class Engine:
+    def __init__(self, *, layers: int, q_heads: int, kv_heads: int, head_dim: int,
+                 block_size: int, dtype: torch.dtype, num_blocks: int, max_pos: int,
+                 theta: float, batch: int, pool: torch.Tensor, device="cuda"):
+        self.L, self.Hq, self.Hkv, self.D, self.B = layers, q_heads, kv_heads, head_dim, block_size
+        self.dtype, self.batch, self.device = dtype, batch, device
+        shape = (layers, num_blocks, kv_heads, block_size, head_dim)
+        self.k_cache = torch.empty(shape, dtype=dtype, device=device)
+        self.v_cache = torch.empty(shape, dtype=dtype, device=device)
+        self.cache = K.Cache(self.k_cache, self.v_cache)
+        self.pool = K.Pool(pool)
+        self.chunk_len = pool.shape[3]
+        self.rope = K.make_rope(theta, head_dim, max_pos, device)
+        self.workspace = K.make_decode_workspace(batch, q_heads, kv_heads, head_dim, device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.decode_variant = 0
+        self.decode_ctas = 0
+
+    # -- single operations ---------------------------------------------------
+    def slot_mapping(self, block_tables, seq, pos, out=None):
+        if out is None:
+            out = torch.empty(pos.numel(), dtype=torch.int64, device=self.device)
+        return K.kvinj_slot_mapping(block_tables, seq, pos, self.cache.num_blocks, self.B, out,
+                                    self.status)
+
+    def inject(self, chunk_ids, start_pos, slots, layer_begin=0, layer_end=None):
+        K.kvinj_inject(self.pool, self.cache, self.rope, chunk_ids, start_pos, slots,
+                       layer_begin, layer_end, self.status)
+
+    def append(self, layer, k_new, v_new, positions, slots, rotate=True):
+        K.kvinj_append(self.cache, self.rope if rotate else None, layer, k_new, v_new,
+                       positions, slots, self.status)
+
+    def decode(self, layer, q, q_pos, block_tables, ctx_lens, out, rotate=True):
+        K.kvinj_paged_decode_ex(self.cache, self.rope if rotate else None, layer, q, q_pos,
+                                block_tables, ctx_lens, out, self.workspace, 0.0, self.status,
+                                None, self.decode_variant, self.decode_ctas)
+
+    # -- one step of the hot path --------------------------------------------
+    def alloc_outputs(self, steps: int) -> torch.Tensor:
+        return torch.empty((steps, self.L, self.batch, self.Hq, self.D), dtype=self.dtype,
+                           device=self.device)
+
+    def step(self, inp: StepInputs, out: torch.Tensor, timer=None):
+        """slot mapping + inject + (append, decode) per step and layer.
+
+        `timer`, when given, is called as timer(kind, stream_event_pair_index)
+        around the inject and decode launches (used for per-kernel timing)."""
+        n_tok = inp.map_pos.numel()
+        slots = self.slot_mapping(inp.block_tables, inp.map_seq, inp.map_pos)
+        n_inj_tok = inp.chunk_ids.numel() * self.chunk_len
+        if timer:
+            timer("inject", 0)
+        self.inject(inp.chunk_ids, inp.start_pos, slots[:n_inj_tok])
+        if timer:
+            timer("inject", 1)
+        steps = inp.q.shape[0]
+        step_slots = slots[n_inj_tok:n_tok].view(steps, self.batch)
+        for s in range(steps):
+            for layer in range(self.L):
+                self.append(layer, inp.k_new[s, layer], inp.v_new[s, layer], inp.q_pos[s],
+                            step_slots[s])
+                if timer:
+                    timer("decode", 0)
+                self.decode(layer, inp.q[s, layer], inp.q_pos[s], inp.block_tables,
+                            inp.ctx_lens[s], out[s, layer])
+                if timer:
+                    timer("decode", 1)
+        return out
+
+    def step_from_host(self, host: StepInputs, dev: StepInputs, out: torch.Tensor,
+                       host_out: torch.Tensor):
+        """End to end: pinned host inputs -> device, step, outputs -> pinned host."""
+        for h, d in zip(host.tensors(), dev.tensors()):
+            d.copy_(h, non_blocking=True)
+        self.step(dev, out)
+        host_out.copy_(out, non_blocking=True)
+        return host_out

@@ -1,0 +1,324 @@
+"""GPU parity of each entry point against the fp64 oracle, element by element,
+on seeded inputs that span several pages, CTAs and a ragged tail; plus the
+edge cases (empty, ragged, single token, invalid indices, workspace size).
+
+Inputs come from the shared seeded generator (workload); expectations only
+from oracle/. Calls go through the C ABI (ctypes binding)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workload as W
+from paged_kv_cache_inject_gb300 import kvinj as K
+from tests.gpu_helpers import assert_decode_close, bits, from_bits, torch_dtype, ulp_distance
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = 0x7FC1  # a NaN pattern no kernel writes
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def gen_bits(seed: int, shape, dt):
+    key = W.stream_key(seed, W.STREAM_POOL)
+    n = int(np.prod(shape))
+    return W.normal_bits(key, np.arange(n, dtype=np.uint64), dt).reshape(shape)
+
+
+def i32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
+
+
+def status_tensor():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+# ---------------------------------------------------------------------------
+# slot mapping
+# ---------------------------------------------------------------------------
+def test_slot_mapping_bit_exact():
+    rng = np.random.default_rng(1)
+    batch, max_blocks, NB, B = 7, 40, 300, 16
+    bt = rng.permutation(NB)[:batch * max_blocks].reshape(batch, max_blocks).astype(np.int32)
+    n = 100_003
+    seq = rng.integers(0, batch, n).astype(np.int32)
+    pos = rng.integers(0, max_blocks * B, n).astype(np.int32)
+    want, st = oracle.slot_mapping(bt, seq, pos, B, NB)
+    assert st == 0
+    out = torch.empty(n, dtype=torch.int64, device="cuda")
+    status = status_tensor()
+    K.kvinj_slot_mapping(i32(bt), i32(seq), i32(pos), NB, B, out, status)
+    assert np.array_equal(out.cpu().numpy(), want)
+    assert status.item() == 0
+
+
+def test_slot_mapping_invalid_entries_flagged():
+    bt = np.array([[3, 7, 1], [2, 9, -1]], np.int32)
+    seq = np.array([0, 1, 5, 0, 1, -1, 0], np.int32)
+    pos = np.array([20, 16, 0, 48, 40, 0, -3], np.int32)
+    want, st = oracle.slot_mapping(bt, seq, pos, 16, 10)
+    out = torch.empty(seq.size, dtype=torch.int64, device="cuda")
+    status = status_tensor()
+    K.kvinj_slot_mapping(i32(bt), i32(seq), i32(pos), 10, 16, out, status)
+    assert np.array_equal(out.cpu().numpy(), want)
+    assert list(want) == [116, 144, -1, -1, -1, -1, -1]
+    assert status.item() == K.ST_BAD_SEQ | K.ST_BAD_POS | K.ST_BAD_BLOCK
+
+
+# ---------------------------------------------------------------------------
+# inject
+# ---------------------------------------------------------------------------
+def _inject_case(D, dt, seed=3):
+    rng = np.random.default_rng(seed)
+    L, Hkv, c, n_chunks, B, NB = 3, 4, 5, 7, 16, 24
+    pool = gen_bits(seed, (n_chunks, L, 2, c, Hkv, D), dt)
+    perm = rng.permutation(NB).astype(np.int32)
+    bt = perm.reshape(2, 12)
+    ids = np.array([3, 0, 6, 3], np.int32)
+    req = np.array([0, 0, 1, 1], np.int32)
+    start = np.array([0, 13, 100, 187], np.int32)  # one chunk straddles a block, one ends the table
+    seq = np.repeat(req, c).astype(np.int32)
+    pos = (start[:, None] + np.arange(c)).reshape(-1).astype(np.int32)
+    slots, st = oracle.slot_mapping(bt, seq, pos, B, NB)
+    assert st == 0
+    return dict(L=L, Hkv=Hkv, c=c, B=B, NB=NB, pool=pool, bt=bt, ids=ids, start=start, seq=seq,
+                pos=pos, slots=slots)
+
+
+@pytest.mark.parametrize("D,dt", [(64, W.BF16), (128, W.BF16), (128, W.FP16), (256, W.BF16)])
+def test_inject_matches_oracle(D, dt):
+    cs = _inject_case(D, dt)
+    L, Hkv, B, NB = cs["L"], cs["Hkv"], cs["B"], cs["NB"]
+    tdt = torch_dtype(dt)
+    theta = 5e5 if D == 128 else 1e4
+    kc = np.full((L, NB, Hkv, B, D), SENTINEL, np.uint16)
+    vc = kc.copy()
+    assert oracle.inject(cs["pool"], cs["ids"], cs["start"], cs["slots"], theta, dt, kc, vc) == 0
+
+    cache = K.Cache(from_bits(np.full_like(kc, SENTINEL), tdt), from_bits(np.full_like(kc, SENTINEL), tdt))
+    pool = K.Pool(from_bits(cs["pool"], tdt))
+    rope = K.make_rope(theta, D, 200)
+    slots_d = torch.empty(cs["pos"].size, dtype=torch.int64, device="cuda")
+    status = status_tensor()
+    K.kvinj_slot_mapping(i32(cs["bt"]), i32(cs["seq"]), i32(cs["pos"]), NB, B, slots_d, status)
+    assert np.array_equal(slots_d.cpu().numpy(), cs["slots"])
+    K.kvinj_inject(pool, cache, rope, i32(cs["ids"]), i32(cs["start"]), slots_d, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    gk, gv = bits(cache.k), bits(cache.v)
+    assert np.array_equal(gv, vc), "V must be a bit copy and nothing else may change"
+    written = kc != SENTINEL
+    assert np.array_equal(gk[~written], kc[~written])
+    d = ulp_distance(gk[written], kc[written])
+    assert d.max() <= 1, f"rotated K beyond one ulp: {d.max()}"
+    assert (d == 0).mean() > 0.99
+
+
+def test_inject_layer_range_and_bad_indices():
+    D, dt = 128, W.BF16
+    cs = _inject_case(D, dt, seed=4)
+    L, Hkv, B, NB = cs["L"], cs["Hkv"], cs["B"], cs["NB"]
+    tdt = torch_dtype(dt)
+    kc = np.full((L, NB, Hkv, B, D), SENTINEL, np.uint16)
+    vc = kc.copy()
+    # layers [1, 2) only; chunk 1 has a bad id, chunk 2 a bad slot on token 0 and chunk 3 runs
+    # past the rope table (max_pos 190: positions 187..191)
+    ids = cs["ids"].copy()
+    ids[1] = 99
+    slots = cs["slots"].copy()
+    slots[2 * cs["c"]] = -1
+    ok_ids = ids.copy()
+    orc_slots = slots.copy()
+    st = oracle.inject(cs["pool"], ok_ids, cs["start"], orc_slots, 1e4, dt, kc, vc,
+                       layer_begin=1, layer_end=2)
+    assert st == oracle.ST_CHUNK | oracle.ST_SLOT
+    # the oracle has no table limit: undo what it wrote past position 189
+    for j in range(len(ids)):
+        for t in range(cs["c"]):
+            if cs["start"][j] + t >= 190 and ids[j] < 7 and slots[j * cs["c"] + t] >= 0:
+                s = slots[j * cs["c"] + t]
+                kc[1, s // B, :, s % B] = SENTINEL
+                vc[1, s // B, :, s % B] = SENTINEL
+    cache = K.Cache(from_bits(np.full_like(kc, SENTINEL), tdt), from_bits(np.full_like(kc, SENTINEL), tdt))
+    pool = K.Pool(from_bits(cs["pool"], tdt))
+    rope = K.make_rope(1e4, D, 190)
+    status = status_tensor()
+    K.kvinj_inject(pool, cache, rope, i32(ids), i32(cs["start"]),
+                   torch.from_numpy(slots).cuda(), 1, 2, status)
+    torch.cuda.synchronize()
+    assert status.item() == K.ST_BAD_CHUNK | K.ST_BAD_SLOT | K.ST_BAD_POS
+    gk, gv = bits(cache.k), bits(cache.v)
+    assert np.array_equal(gv, vc)
+    assert ulp_distance(gk, kc).max() <= 1
+    assert np.all(gk[0] == SENTINEL) and np.all(gk[2] == SENTINEL)
+
+
+def test_inject_empty_is_noop():
+    D = 64
+    cache = K.Cache(torch.zeros((1, 2, 1, 16, D), dtype=torch.bfloat16, device="cuda"),
+                    torch.zeros((1, 2, 1, 16, D), dtype=torch.bfloat16, device="cuda"))
+    pool = K.Pool(torch.ones((1, 1, 2, 4, 1, D), dtype=torch.bfloat16, device="cuda"))
+    rope = K.make_rope(1e4, D, 16)
+    e32 = torch.empty(0, dtype=torch.int32, device="cuda")
+    K.kvinj_inject(pool, cache, rope, e32, e32, torch.empty(0, dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    assert not cache.k.any() and not cache.v.any()
+
+
+# ---------------------------------------------------------------------------
+# append
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("D,dt,rotate", [(128, W.BF16, True), (64, W.FP16, True),
+                                         (128, W.BF16, False), (256, W.FP16, True)])
+def test_append_matches_oracle(D, dt, rotate):
+    rng = np.random.default_rng(5)
+    L, Hkv, B, NB, n = 2, 3, 16, 9, 37
+    tdt = torch_dtype(dt)
+    kn = gen_bits(10 + D, (n, Hkv, D), dt)
+    vn = gen_bits(20 + D, (n, Hkv, D), dt)
+    slots = rng.permutation(NB * B)[:n].astype(np.int64)
+    pos = rng.integers(0, 4000, n).astype(np.int32)
+    kc = np.full((L, NB, Hkv, B, D), SENTINEL, np.uint16)
+    vc = kc.copy()
+    assert oracle.append(kc, vc, 1, kn, vn, pos, slots, 5e5, dt, rotate=rotate) == 0
+    cache = K.Cache(from_bits(np.full_like(kc, SENTINEL), tdt), from_bits(np.full_like(kc, SENTINEL), tdt))
+    rope = K.make_rope(5e5, D, 4000) if rotate else None
+    status = status_tensor()
+    K.kvinj_append(cache, rope, 1, from_bits(kn, tdt), from_bits(vn, tdt), i32(pos),
+                   torch.from_numpy(slots).cuda(), status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    gk, gv = bits(cache.k), bits(cache.v)
+    assert np.array_equal(gv, vc)
+    d = ulp_distance(gk, kc)
+    assert d.max() <= (1 if rotate else 0)
+
+
+# ---------------------------------------------------------------------------
+# paged decode
+# ---------------------------------------------------------------------------
+def _decode_case(D, G, dt, ctx, Hkv=2, L=2, seed=7, spare=3):
+    rng = np.random.default_rng(seed)
+    B = 16
+    ctx = np.asarray(ctx, np.int32)
+    pages = -(-ctx // B)
+    NB = int(pages.sum()) + spare
+    max_blocks = int(pages.max()) + 2
+    perm = rng.permutation(NB).astype(np.int32)
+    bt = np.full((ctx.size, max_blocks), -1, np.int32)
+    o = 0
+    for r, p in enumerate(pages):
+        bt[r, :p] = perm[o:o + p]
+        o += p
+    kc = gen_bits(seed, (L, NB, Hkv, B, D), dt)
+    vc = gen_bits(seed + 1, (L, NB, Hkv, B, D), dt)
+    q = gen_bits(seed + 2, (ctx.size, Hkv * G, D), dt)
+    return kc, vc, q, bt
+
+
+def _run_decode(kc, vc, q, bt, ctx, q_pos, dt, layer, theta, rope_max, variant=0, ctas=0,
+                rotate=True, ws_bytes=None, status=None):
+    tdt = torch_dtype(dt)
+    D = kc.shape[-1]
+    cache = K.Cache(from_bits(kc, tdt), from_bits(vc, tdt))
+    rope = K.make_rope(theta, D, rope_max) if rotate else None
+    batch, Hq, _ = q.shape
+    Hkv = kc.shape[2]
+    n = K.kvinj_decode_workspace_size(batch, Hq, Hkv, D) if ws_bytes is None else ws_bytes
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    out = torch.full((batch, Hq, D), float("nan"), dtype=tdt, device="cuda")
+    K.kvinj_paged_decode_ex(cache, rope, layer, from_bits(q, tdt), i32(q_pos), i32(bt), i32(ctx),
+                            out, ws, 0.0, status, None, variant, ctas)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64), ws
+
+
+DECODE_SHAPES = [(64, 1, W.BF16), (64, 2, W.BF16), (128, 4, W.BF16), (128, 8, W.BF16),
+                 (128, 1, W.FP16), (128, 4, W.FP16), (64, 8, W.FP16), (128, 2, W.BF16)]
+
+
+@pytest.mark.parametrize("D,G,dt", DECODE_SHAPES)
+@pytest.mark.parametrize("ctas", [0, 1, 5, 37])
+def test_decode_matches_oracle(D, G, dt, ctas):
+    ctx = [1, 16, 17, 250, 611]
+    kc, vc, q, bt = _decode_case(D, G, dt, ctx)
+    ctx = np.array(ctx, np.int32)
+    q_pos = ctx - 1
+    theta = 5e5
+    status = status_tensor()
+    got, _ = _run_decode(kc, vc, q, bt, ctx, q_pos, dt, 1, theta, 1000, ctas=ctas, status=status)
+    assert status.item() == 0
+    want, st = oracle.paged_decode(kc, vc, 1, q, q_pos, bt, ctx, theta, dt)
+    assert st == 0
+    assert_decode_close(got, want, f"D{D} G{G} dt{dt} ctas{ctas}")
+
+
+def test_decode_long_context_and_unrotated_query():
+    D, G, dt = 128, 8, W.BF16
+    ctx = np.array([9000, 3, 4097], np.int32)
+    kc, vc, q, bt = _decode_case(D, G, dt, ctx, Hkv=1, L=1, seed=11)
+    got, _ = _run_decode(kc, vc, q, bt, ctx, ctx - 1, dt, 0, 5e5, 9000)
+    want, _ = oracle.paged_decode(kc, vc, 0, q, ctx - 1, bt, ctx, 5e5, dt)
+    assert_decode_close(got, want, "long")
+    got, _ = _run_decode(kc, vc, q, bt, ctx, ctx - 1, dt, 0, 5e5, 9000, rotate=False)
+    want, _ = oracle.paged_decode(kc, vc, 0, q, ctx - 1, bt, ctx, 5e5, dt, rotate_q=False)
+    assert_decode_close(got, want, "unrotated")
+
+
+def test_decode_deterministic_and_workspace_reusable():
+    D, G, dt = 128, 4, W.BF16
+    ctx = np.array([700, 33, 1500, 16], np.int32)
+    kc, vc, q, bt = _decode_case(D, G, dt, ctx, seed=12)
+    tdt = torch_dtype(dt)
+    cache = K.Cache(from_bits(kc, tdt), from_bits(vc, tdt))
+    rope = K.make_rope(5e5, D, 2000)
+    ws = K.make_decode_workspace(4, 4 * 2, 2, D)
+    outs = []
+    for _ in range(3):
+        out = torch.empty((4, 8, D), dtype=tdt, device="cuda")
+        K.kvinj_paged_decode(cache, rope, 0, from_bits(q, tdt), i32(ctx - 1), i32(bt), i32(ctx),
+                             out, ws)
+        outs.append(bits(out))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    counters = ws[:4 * 2 * 4].view(torch.int32).cpu().numpy()
+    assert not counters.any(), "split counters must be left at zero"
+
+
+def test_decode_invalid_context_and_block():
+    D, G, dt = 64, 2, W.BF16
+    ctx_ok = [40, 50, 60]
+    kc, vc, q, bt = _decode_case(D, G, dt, ctx_ok, seed=13)
+    ctx = np.array([0, 50, 10 ** 6], np.int32)
+    status = status_tensor()
+    got, _ = _run_decode(kc, vc, q, bt, ctx, np.array([0, 49, 0], np.int32), dt, 0, 1e4, 100,
+                         status=status)
+    assert status.item() == K.ST_BAD_CTX
+    assert not got[0].any() and not got[2].any()
+    want, _ = oracle.paged_decode(kc, vc, 0, q[1:2], [49], bt[1:2], [50], 1e4, dt)
+    assert_decode_close(got[1:2], want, "valid request next to invalid ones")
+    # a block-table entry outside the cache: flagged, other requests unaffected
+    bt2 = bt.copy()
+    bt2[0, 1] = kc.shape[1] + 5
+    status = status_tensor()
+    got, _ = _run_decode(kc, vc, q, bt2, np.array(ctx_ok, np.int32), np.array(ctx_ok) - 1, dt, 0,
+                         1e4, 100, status=status)
+    assert status.item() == K.ST_BAD_BLOCK
+    want, _ = oracle.paged_decode(kc, vc, 0, q[1:], np.array(ctx_ok[1:]) - 1, bt[1:], ctx_ok[1:],
+                                  1e4, dt)
+    assert_decode_close(got[1:], want, "requests after a bad block")
+
+
+def test_decode_workspace_too_small_is_refused():
+    D, G, dt = 64, 1, W.BF16
+    kc, vc, q, bt = _decode_case(D, G, dt, [20], seed=14)
+    with pytest.raises(K.KvinjError) as e:
+        _run_decode(kc, vc, q, bt, np.array([20], np.int32), np.array([19], np.int32), dt, 0, 1e4,
+                    40, ws_bytes=64)
+    assert e.value.code == K.KVINJ_EWORKSPACE
