@@ -261,11 +261,20 @@ def run_gpu(args):
     __graft_entry__.build()
 
     cfg = W.CONFIGS[args.config]
+    if args.layers:
+        cfg = cfg.scaled(layers=args.layers)  # batch structure does not depend on L
     wl = W.make_workload(cfg, seed=cfg.seed + 1000 * rank)  # independent replica per rank
-    eng = stage.make_engine(wl, dev)
+    remap = None
+    if args.compact_pool:
+        pool, remap = stage.compact_pool(wl, dev)
+        eng = stage.make_engine(wl, dev, pool=pool)
+    else:
+        eng = stage.make_engine(wl, dev)
     eng.decode_variant = args.variant
     stage.fill_context(eng, wl, dev)
     inp = stage.step_inputs(wl, dev)
+    if remap is not None:
+        inp.chunk_ids.copy_(torch.from_numpy(remap).to(dev))
     out = eng.alloc_outputs(cfg.steps)
     nbytes = stage.algorithmic_bytes(wl)
     stream = torch.cuda.current_stream()
@@ -282,25 +291,45 @@ def run_gpu(args):
     if eng.status.item() != 0:
         raise RuntimeError(f"device status {eng.status.item():#x} after warm-up")
 
-    # timed region: K steps, per-kernel events on the launching stream
-    ev = {"inject": [], "decode": []}
-    pending = {}
+    # One CUDA graph per timed step (the decode loop is launch-bound from
+    # Python otherwise), each with its own timing events around the inject
+    # and decode launches, recorded as graph nodes on the launching stream.
+    def make_timer(store, external):
+        pending = {}
 
-    def timer(kind, which):
-        e = torch.cuda.Event(enable_timing=True)
-        e.record(stream)
-        if which == 0:
-            pending[kind] = e
-        else:
-            ev[kind].append((pending.pop(kind), e))
+        def timer(kind, which):
+            e = torch.cuda.Event(enable_timing=True, external=external)
+            e.record()
+            if which == 0:
+                pending[kind] = e
+            else:
+                store[kind].append((pending.pop(kind), e))
+        return timer
 
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        external_ok = not args.no_graph
+    except TypeError:
+        external_ok = False
+    graphs, stores = [], []
+    if external_ok:
+        for _ in range(args.steps):
+            store = {"inject": [], "decode": []}
+            graphs.append(eng.capture(inp, out, timer=make_timer(store, True)))
+            stores.append(store)
+        for _ in range(args.warmup):
+            graphs[0].replay()
     barrier()
+    eager_store = {"inject": [], "decode": []}
     with ClockSampler(local) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
-        for _ in range(args.steps):
-            eng.step(inp, out, timer=timer)
+        for k in range(args.steps):
+            if external_ok:
+                graphs[k].replay()
+            else:
+                eng.step(inp, out, timer=make_timer(eager_store, False))
         t_end.record(stream)
         barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
@@ -310,6 +339,10 @@ def run_gpu(args):
         elapsed_ms = float(t.item())
     ms_step = elapsed_ms / args.steps
     value = ws * nbytes["total"] / (ms_step * 1e-3) / 1e9
+    ev = {"inject": [], "decode": []}
+    for st in (stores if external_ok else [eager_store]):
+        for kind in ev:
+            ev[kind].extend(st[kind])
 
     dec_ms = [a.elapsed_time(b) for a, b in ev["decode"]]
     inj_ms = [a.elapsed_time(b) for a, b in ev["inject"]]
@@ -327,14 +360,15 @@ def run_gpu(args):
     if not args.no_e2e:
         host = stage.pinned_copy(inp)
         host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        g0 = graphs[0] if graphs else None
         for _ in range(max(1, args.warmup)):
-            eng.step_from_host(host, inp, out, host_out)
+            eng.step_from_host(host, inp, out, host_out, g0)
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.steps):
-            eng.step_from_host(host, inp, out, host_out)
+            eng.step_from_host(host, inp, out, host_out, g0)
         e1.record(stream)
         barrier()
         e_ms = e0.elapsed_time(e1) / args.steps
@@ -373,7 +407,10 @@ def run_gpu(args):
                    "decode_steps": cfg.steps, "parallelism": f"replicas x{ws}",
                    "l2": (f"inputs larger than L2: {nbytes['total'] / 1e9:.2f} GB touched per "
                           f"step; no flush"),
-                   "decode_variant": args.variant},
+                   "decode_variant": args.variant,
+                   "launch": "cuda graph per step" if external_ok else "eager",
+                   "pool": ("drawn chunks only" if args.compact_pool else
+                            f"full, {cfg.pool_bytes / 1e9:.1f} GB resident")},
         "parts": {
             "inject": {"tokens_per_s": inj_tok_s, "gbs": inj_gbs, "ms": inj_avg,
                        "pct_of_8tbs": 100 * inj_gbs / NOMINAL_HBM_GBS,
@@ -407,6 +444,11 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--variant", type=int, default=0, help="decode kernel: 0 auto, 1 FMA, 2 mma")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly from Python")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the layer count (small profiling cases only)")
+    ap.add_argument("--compact-pool", action="store_true",
+                    help="keep only the drawn chunks resident (small profiling cases only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

@@ -185,9 +185,10 @@ int kvinj_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t
                        kvinj_stream_t stream);
 
 /* Same as kvinj_paged_decode with an explicit kernel choice:
- * variant 0 = automatic, 1 = CUDA-core FMA kernel, 2 = tensor-core (mma)
- * kernel. `ctas` > 0 overrides the grid size (1 .. number of workspace
- * slots); 0 = one CTA per SM. */
+ * variant 0 = automatic, 1 = CUDA-core FMA kernel (G in {1, 2, 4, 8}),
+ * 2 = tensor-core mma.sync kernel (G in {1, 2, 4, 8, 16}). `ctas` > 0
+ * overrides the grid size (1 .. 2 x the SM count, the workspace slots);
+ * 0 = one CTA per SM. */
 int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
                           int32_t num_q_heads, const void *q, const int32_t *q_pos,
                           const int32_t *block_tables, int32_t max_blocks,

@@ -25,9 +25,14 @@ int num_sms() {
 }
 
 size_t decode_partial_floats(int G, int D) { return (size_t)G * (size_t)(D + 2); }
-int decode_max_ctas() { return 4 * num_sms(); }
-size_t decode_counters_bytes(int batch, int Hkv) {
-  return (((size_t)batch * Hkv * sizeof(int)) + 255) & ~size_t(255);
+int decode_max_ctas() { return 2 * num_sms(); }
+int decode_head_group(int Hkv) {
+  int hg = 8;
+  while (hg > 1 && Hkv % hg) hg >>= 1;
+  return hg;
+}
+size_t decode_desc_bytes() {
+  return (((size_t)decode_max_ctas() * 8 * sizeof(int)) + 255) & ~size_t(255);
 }
 
 }  // namespace kvinj
@@ -82,15 +87,16 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2-D view of one cache array: rows of D elements, L*num_blocks*Hkv*16 rows;
-// box 16 rows x 64 elements (128 bytes), 128-byte swizzle
-int make_cache_map(CUtensorMap *m, void *base, const kvinj_cache *c) {
+// box 64 elements (128 bytes) x HG*16 rows (HG kv heads of one block),
+// 128-byte swizzle
+int make_cache_map(CUtensorMap *m, void *base, const kvinj_cache *c, int HG) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return KVINJ_ECUDA;
   const uint64_t rows = (uint64_t)c->num_layers * (uint64_t)c->num_blocks *
                         (uint64_t)c->num_kv_heads * (uint64_t)c->block_size;
   cuuint64_t dims[2] = {(cuuint64_t)c->head_dim, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)c->head_dim * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)c->block_size};
+  cuuint32_t box[2] = {64, (cuuint32_t)(c->block_size * HG)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -216,8 +222,9 @@ size_t kvinj_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
       head_dim <= 0)
     return 0;
   const int G = num_q_heads / num_kv_heads;
-  return decode_counters_bytes(batch, num_kv_heads) +
-         (size_t)2 * decode_max_ctas() * decode_partial_floats(G, head_dim) * sizeof(float);
+  const int HG = decode_head_group(num_kv_heads);
+  return decode_desc_bytes() +
+         (size_t)2 * decode_max_ctas() * HG * decode_partial_floats(G, head_dim) * sizeof(float);
 }
 
 int kvinj_decode_workspace_init(void *workspace, size_t ws_bytes, kvinj_stream_t stream) {
@@ -244,9 +251,9 @@ int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int3
   if (rope && !q_pos) return KVINJ_EINVAL;
   if (!aligned16(q) || !aligned16(out)) return KVINJ_EINVAL;
   if (variant < 0 || variant > 2) return KVINJ_EINVAL;
-  if (variant == 0) variant = 1;
+  if (variant == 0) variant = G >= 4 ? 2 : 1;
   if (variant == 1 && !(G == 1 || G == 2 || G == 4 || G == 8)) return KVINJ_EUNSUPPORTED;
-  if (variant == 2) return KVINJ_EUNSUPPORTED;
+  if (variant == 2 && !(G == 1 || G == 2 || G == 4 || G == 8 || G == 16)) return KVINJ_EUNSUPPORTED;
   if ((int64_t)batch * Hkv * max_blocks >= (int64_t)1 << 31) return KVINJ_EUNSUPPORTED;
   if (batch > 4096) return KVINJ_EUNSUPPORTED;  // per-request prefix sums live in shared memory
   if ((int64_t)cache->num_layers * cache->num_blocks * Hkv * 16 >= (int64_t)1 << 31)
@@ -256,9 +263,10 @@ int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int3
   if (ctas < 0 || ctas > max_ctas) return KVINJ_EINVAL;
   if (ctas == 0) ctas = num_sms();
 
+  const int HG = decode_head_group(Hkv);
   CUtensorMap tmK, tmV;
-  if ((rc = make_cache_map(&tmK, cache->k, cache))) return rc;
-  if ((rc = make_cache_map(&tmV, cache->v, cache))) return rc;
+  if ((rc = make_cache_map(&tmK, cache->k, cache, HG))) return rc;
+  if ((rc = make_cache_map(&tmV, cache->v, cache, HG))) return rc;
 
   DecodeArgs a;
   a.q = static_cast<const uint16_t *>(q);
@@ -268,9 +276,8 @@ int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int3
   a.rope = rope ? static_cast<const float4 *>(rope->table) : nullptr;
   a.max_pos = rope ? rope->max_pos : 0;
   a.out = static_cast<uint16_t *>(out);
-  a.counters = static_cast<int *>(workspace);
-  a.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                         decode_counters_bytes(batch, Hkv));
+  a.desc = static_cast<int *>(workspace);
+  a.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + decode_desc_bytes());
   a.status = dev_status;
   a.batch = batch;
   a.Hq = num_q_heads;
@@ -280,7 +287,7 @@ int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int3
   a.num_blocks = cache->num_blocks;
   const double sc = scale > 0.f ? (double)scale : 1.0 / sqrt((double)D);
   a.scale_log2 = (float)(sc * 1.4426950408889634);
-  return cuda_rc(launch_decode(a, tmK, tmV, D, G, cache->dtype, variant, ctas,
+  return cuda_rc(launch_decode(a, tmK, tmV, D, G, HG, cache->dtype, variant, ctas,
                                (cudaStream_t)stream));
 }
 
@@ -315,8 +322,9 @@ const char *kvinj_strerror(int code) {
 
 namespace kvinj {
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                          int D, int G, int dtype, int variant, int ctas, cudaStream_t s) {
-  if (variant == 1) return launch_decode_ffma(a, tmK, tmV, D, G, dtype, ctas, s);
+                          int D, int G, int HG, int dtype, int variant, int ctas, cudaStream_t s) {
+  if (variant == 1) return launch_decode_ffma(a, tmK, tmV, D, G, HG, dtype, ctas, s);
+  if (variant == 2) return launch_decode_mma(a, tmK, tmV, D, G, HG, dtype, ctas, s);
   return cudaErrorInvalidValue;
 }
 }  // namespace kvinj

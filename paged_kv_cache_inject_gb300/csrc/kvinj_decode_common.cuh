@@ -1,8 +1,27 @@
-// kvinj_decode_common.cuh -- parts of the split-K paged decode shared by the
-// CUDA-core and tensor-core consumers: shared-memory layout, the prologue
-// (pages per request, prefix sums, this CTA's range), the TMA producer warp,
-// the query load/rotation, and the end-of-piece merge with the in-kernel
-// combine of pieces that several CTAs produced.
+// kvinj_decode_common.cuh -- the parts of the split-K paged decode shared by
+// the CUDA-core and tensor-core consumers: shared-memory layout, prologue
+// (units per request, prefix sums, this CTA's range), the TMA producer warp,
+// piece lookup, and the end-of-piece protocol (final outputs, or partial
+// softmax states combined in-kernel by the CTA that finishes a segment last).
+//
+// Work unit. A physical block of the cache holds, per layer, the 16 tokens
+// of every kv head contiguously ([Hkv][16][D] for K, the same for V). The
+// unit of work is one block of one group of HG consecutive kv heads: HG*16
+// rows of K and of V, contiguous, fetched with two TMA boxes each (16 KiB
+// boxes for HG = 8, D = 128). Streaming units of 16-32 KiB reaches the HBM
+// rate where 4 KiB pages of a single head do not. Consumer warp w owns kv
+// head hg*HG + w of the group and every unit passes through all HG warps.
+//
+// Segments and pieces. The units of (request r, head group hg) form a
+// segment of ceil(C_r/16) units. Units are flattened request-major and cut
+// into gridDim.x equal contiguous ranges, one per CTA. A segment inside one
+// CTA range is finished there; a segment cut by range boundaries leaves one
+// partial softmax state per piece in the workspace. The CTA whose range holds
+// the last unit of a cut segment records a descriptor of it, and a second,
+// small kernel launched after this one on the same stream combines the
+// pieces (stream order makes every partial visible to it). The streaming
+// kernel thus needs no fence, atomic or counter, and nothing waits on
+// another CTA.
 #pragma once
 
 #include <math.h>
@@ -12,26 +31,29 @@
 
 namespace kvinj {
 
-constexpr int BLK = 16;                  // tokens per page (block size)
+constexpr int BLK = 16;                      // tokens per block
 constexpr int DECODE_MAX_SMEM = 227 * 1024;  // opt-in dynamic shared memory per CTA
-constexpr int BOX_BYTES = BLK * 64 * 2;  // one TMA box: 16 rows x 64 elements
 
-template <int D_, int G_, int NW_, int S_>
+template <int D_, int G_, int HG_, int S_, int QB_ = 0>
 struct DecodeLayout {
-  static constexpr int D = D_, G = G_, NW = NW_, S = S_;
-  static constexpr int NBOX = D / 64;
-  static constexpr int PAGE_BYTES = NBOX * BOX_BYTES;  // K (or V) page of one head
-  static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;   // K page then V page
-  static constexpr int off_stage = 0;                  // 1024-byte aligned
-  static constexpr int off_bar = S * STAGE_BYTES;      // full[S], empty[S]
-  static constexpr int off_valid = off_bar + 2 * S * 8;
-  static constexpr int off_flags = off_valid + S * 4;  // [0] abort [1] last [8..40) scan
-  static constexpr int off_p = off_flags + 256;        // float [NW][16][G]
-  static constexpr int off_alpha = off_p + NW * 16 * G * 4;
-  static constexpr int off_mm = off_alpha + NW * G * 4;  // float [NW][G]
-  static constexpr int off_ml = off_mm + NW * G * 4;     // float [NW][G]
-  static constexpr int off_macc = off_ml + NW * G * 4;   // float [NW][G][D]
-  static constexpr int off_pre = off_macc + NW * G * D * 4;
+  static constexpr int D = D_, G = G_, HG = HG_, S = S_;
+  static constexpr int QB = QB_;                        // q staging buffers (0 = none)
+  static constexpr int NBOX = D / 64;                   // 64-element (128-byte) column boxes
+  static constexpr int BOXB = HG * BLK * 128;           // bytes of one box: HG*16 rows
+  static constexpr int UNIT_BYTES = NBOX * BOXB;        // K (or V) of one unit
+  static constexpr int STAGE_BYTES = 2 * UNIT_BYTES;    // K then V
+  static constexpr int Q_BYTES = HG * G * D * 2;        // q rows of one head group
+  static constexpr int T_BYTES = (D / 2) * 16;          // one RoPE table row
+  static constexpr int off_stage = 0;                   // 1024-byte aligned
+  static constexpr int off_q = S * STAGE_BYTES;         // [QB][Q_BYTES]
+  static constexpr int off_t = off_q + QB * Q_BYTES;    // [QB][T_BYTES]
+  static constexpr int off_bar = off_t + QB * T_BYTES;  // full[S], empty[S], qfull[QB], qempty[QB]
+  static constexpr int off_valid = off_bar + (2 * S + 2 * QB) * 8;
+  static constexpr int off_qinfo = off_valid + S * 4;   // [QB] q position (-1: no rotation)
+  static constexpr int off_flags = off_qinfo + 16;      // [0] abort [1] last [8..40) scan
+  static constexpr int off_scratch = off_flags + 256;   // per warp: p[16][G], alpha[G]
+  static constexpr int SCRATCH_FLOATS = 17 * G;
+  static constexpr int off_pre = off_scratch + HG * SCRATCH_FLOATS * 4;
   static size_t bytes(int batch) { return (size_t)off_pre + (size_t)(batch + 1) * 4 + 1024; }
 };
 
@@ -40,30 +62,38 @@ __device__ __forceinline__ uint8_t *align_smem(uint8_t *p) {
   return reinterpret_cast<uint8_t *>((a + 1023) & ~uintptr_t(1023));
 }
 
+// byte offset, inside a unit's K (or V) half, of 16-byte chunk `chunk`
+// (0 .. D/8-1) of token `tok` of the warp's head `w`: the 128-byte swizzle
+// of the TMA boxes XORs the chunk index with the row index mod 8
+template <int BOXB>
+__device__ __forceinline__ uint32_t unit_off(int w, int chunk, int tok) {
+  return (chunk >> 3) * BOXB + (w * BLK + tok) * 128 + (((chunk & 7) ^ (tok & 7)) << 4);
+}
+
 struct CtaRange {
-  int b0, b1;   // this CTA's pages [b0, b1) of the flattened page sequence
-  int n_eff;    // CTAs that received pages
-  int Ptot;     // total pages
+  int b0, b1;  // this CTA's units [b0, b1) of the flattened unit sequence
+  int n_eff;   // CTAs that received units
+  int Ptot;    // total units
 };
 
 __device__ __forceinline__ int range_begin(int c, const CtaRange &rg) {
   return (int)((int64_t)c * rg.Ptot / rg.n_eff);
 }
-// the CTA whose range holds page P
+// the CTA whose range holds unit P
 __device__ __forceinline__ int cta_of(int P, const CtaRange &rg) {
   return (int)(((int64_t)(P + 1) * rg.n_eff - 1) / rg.Ptot);
 }
 
 struct Piece {
-  int r, h;        // request, kv head
-  int pg0;         // first page (within the request) of this piece
-  int ctx;         // context length of the request
-  int seg_start;   // flattened index of the segment's first page
-  int seg_end;     // one past its last page
-  int end;         // one past this piece's last page (<= seg_end)
+  int r, hg;      // request, head group
+  int pg0;        // first block (within the request) of this piece
+  int ctx;        // context length of the request
+  int seg_start;  // flattened index of the segment's first unit
+  int seg_end;    // one past its last unit
+  int end;        // one past this piece's last unit (<= seg_end)
 };
 
-// largest r with pre[r] <= P (requests without pages have pre[r] == pre[r+1])
+// largest r with pre[r] <= P (requests without units have pre[r] == pre[r+1])
 __device__ __forceinline__ int find_request(const int *pre, int batch, int P) {
   int lo = 0, hi = batch - 1;
   while (lo < hi) {
@@ -74,18 +104,42 @@ __device__ __forceinline__ int find_request(const int *pre, int batch, int P) {
   return lo;
 }
 
-__device__ __forceinline__ Piece find_piece(const DecodeArgs &a, const int *pre, int P, int b1) {
+__device__ __forceinline__ Piece find_piece(const DecodeArgs &a, const int *pre, int ngrp, int P,
+                                            int b1) {
   Piece pc;
   pc.r = find_request(pre, a.batch, P);
-  const int pages = (pre[pc.r + 1] - pre[pc.r]) / a.Hkv;
+  const int pages = (pre[pc.r + 1] - pre[pc.r]) / ngrp;
   const int off = P - pre[pc.r];
-  pc.h = off / pages;
-  pc.pg0 = off - pc.h * pages;
-  pc.seg_start = pre[pc.r] + pc.h * pages;
+  pc.hg = off / pages;
+  pc.pg0 = off - pc.hg * pages;
+  pc.seg_start = pre[pc.r] + pc.hg * pages;
   pc.seg_end = pc.seg_start + pages;
   pc.end = min(b1, pc.seg_end);
   pc.ctx = a.context_lens[pc.r];
   return pc;
+}
+
+// Descriptor of the cut segment (if any) whose last unit lies in this CTA's
+// range: only the segment holding the range's first unit can have started
+// before the range. Written by thread 0 of every CTA of the grid (CTAs
+// without units write "none").
+constexpr int DESC_INTS = 8;  // valid, r, hg, seg_start, seg_end, n_eff, Ptot, -
+__device__ __forceinline__ void write_descriptor(const DecodeArgs &a, const int *pre, int ngrp,
+                                                 const CtaRange *rg) {
+  int *d = a.desc + blockIdx.x * DESC_INTS;
+  if (!rg) {
+    d[0] = 0;
+    return;
+  }
+  const Piece pc = find_piece(a, pre, ngrp, rg->b0, rg->b1);
+  const bool ends_cut = pc.seg_start < rg->b0 && pc.seg_end <= rg->b1;
+  d[0] = ends_cut ? 1 : 0;
+  d[1] = pc.r;
+  d[2] = pc.hg;
+  d[3] = pc.seg_start;
+  d[4] = pc.seg_end;
+  d[5] = rg->n_eff;
+  d[6] = rg->Ptot;
 }
 
 __device__ __forceinline__ int valid_pages(const DecodeArgs &a, int r) {
@@ -93,9 +147,9 @@ __device__ __forceinline__ int valid_pages(const DecodeArgs &a, int r) {
   return (c > 0 && c <= a.max_blocks * BLK) ? (c + BLK - 1) / BLK : 0;
 }
 
-// Pages per request -> prefix sums pre[0..batch] (in pages x Hkv), this CTA's
-// range, barrier set-up. CTA 0 also zeroes the output of requests whose
-// context length is invalid. Returns false when this CTA has no pages.
+// Units per request -> prefix sums pre[0..batch], this CTA's range, barrier
+// set-up. CTA 0 also zeroes the output of requests whose context length is
+// invalid. Returns false when this CTA has no units.
 template <class Lay, int NT>
 __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) {
   int *pre = reinterpret_cast<int *>(sm + Lay::off_pre);
@@ -103,12 +157,13 @@ __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) 
   int *ws = flags + 8;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NWARP = NT / 32;
+  const int ngrp = a.Hkv / Lay::HG;
   int carry = 0;
   for (int base = 0; base < a.batch; base += NT) {
     const int r = base + tid;
     int v = 0;
     if (r < a.batch) {
-      v = valid_pages(a, r) * a.Hkv;
+      v = valid_pages(a, r) * ngrp;
       if (v == 0 && blockIdx.x == 0) {
         uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t)r * a.Hq * Lay::D);
         for (int i = 0; i < a.Hq * Lay::D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
@@ -142,14 +197,22 @@ __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) 
   __syncthreads();
   rg.Ptot = pre[a.batch];
   rg.n_eff = min((int)gridDim.x, rg.Ptot);
-  if ((int)blockIdx.x >= rg.n_eff) return false;
+  if ((int)blockIdx.x >= rg.n_eff) {
+    if (tid == 0) write_descriptor(a, pre, ngrp, nullptr);
+    return false;
+  }
   rg.b0 = range_begin(blockIdx.x, rg);
   rg.b1 = range_begin(blockIdx.x + 1, rg);
+  if (tid == 0) write_descriptor(a, pre, ngrp, &rg);
   if (tid == 0) {
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + Lay::off_bar);
     for (int s = 0; s < Lay::S; ++s) {
-      mbar_init(full + s, 1);
-      mbar_init(full + Lay::S + s, 1);
+      mbar_init(full + s, 1);                 // the producer's arrive + the TMA bytes
+      mbar_init(full + Lay::S + s, Lay::HG);  // every consumer warp releases
+    }
+    for (int b = 0; b < Lay::QB; ++b) {
+      mbar_init(full + 2 * Lay::S + b, 1);
+      mbar_init(full + 2 * Lay::S + Lay::QB + b, Lay::HG);
     }
     flags[0] = 0;
     flags[1] = 0;
@@ -159,58 +222,92 @@ __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) 
   return true;
 }
 
-// Producer warp: stream this CTA's pages (K page then V page of one head)
-// into the stage ring. Block-table entries are fetched one per lane, a batch
-// of 32 ahead of their use. Lane 0 issues the TMA copies.
+// Producer warp: stream this CTA's units into the stage ring. Block-table
+// entries are fetched one per lane, a batch of 32 ahead of their use; lane 0
+// issues the copies (NBOX boxes of K and NBOX boxes of V per unit).
 template <class Lay>
 __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
                                 const CUtensorMap &tmV, uint8_t *sm, const CtaRange &rg,
                                 int lane) {
-  constexpr int S = Lay::S, NBOX = Lay::NBOX;
+  constexpr int S = Lay::S, NBOX = Lay::NBOX, HG = Lay::HG;
   uint64_t *full = reinterpret_cast<uint64_t *>(sm + Lay::off_bar);
   uint64_t *empty = full + S;
   volatile int *flags = reinterpret_cast<volatile int *>(sm + Lay::off_flags);
   int *valid = reinterpret_cast<int *>(sm + Lay::off_valid);
   const int *pre = reinterpret_cast<const int *>(sm + Lay::off_pre);
   uint8_t *stages = sm + Lay::off_stage;
+  const int ngrp = a.Hkv / HG;
   if (lane == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
   const int n = rg.b1 - rg.b0;
-  // lookup of page g0 + lane: the block-table load is issued here and
-  // consumed one batch later
-  auto start_lookup = [&](int gi, int &blk, int &h) {
+  // lookup of unit g0 + lane: block-table entry (and, when q is staged, the
+  // request's q position); the loads are consumed one batch later
+  auto start_lookup = [&](int gi, int &blk, int &hg, int &rq, int &first, int &qp) {
     blk = -1;
-    h = 0;
+    hg = 0;
+    rq = 0;
+    first = 0;
+    qp = -1;
     if (gi < n) {
       const int P = rg.b0 + gi;
       const int r = find_request(pre, a.batch, P);
-      const int pages = (pre[r + 1] - pre[r]) / a.Hkv;
+      const int pages = (pre[r + 1] - pre[r]) / ngrp;
       const int off = P - pre[r];
-      h = off / pages;
-      const int pg = off - h * pages;
+      hg = off / pages;
+      const int pg = off - hg * pages;
+      rq = r;
+      first = (gi == 0 || pg == 0) ? 1 : 0;  // first unit of a piece
       blk = a.block_tables[(int64_t)r * a.max_blocks + pg];
+      if (Lay::QB && first && a.rope) qp = a.q_pos[r];
     }
   };
-  int blk, h;
-  start_lookup(lane, blk, h);
-  int issued = 0;
+  int blk, hg, rq, first, qp;
+  start_lookup(lane, blk, hg, rq, first, qp);
+  int issued = 0, pieces = 0;
   bool aborted = false;
   for (int g0 = 0; g0 < n && !aborted; g0 += 32) {
-    int ok = (blk >= 0 && blk < a.num_blocks) ? 1 : 0;
+    const int ok = (blk >= 0 && blk < a.num_blocks) ? 1 : 0;
     if (!ok && g0 + lane < n) report(a.status, KVINJ_ST_BAD_BLOCK);
-    const int row0 =
-        (int)((((int64_t)a.layer * a.num_blocks + (ok ? blk : 0)) * a.Hkv + h) * BLK);
-    int nblk, nh;
-    start_lookup(g0 + 32 + lane, nblk, nh);
+    const int row0 = (int)((((int64_t)a.layer * a.num_blocks + (ok ? blk : 0)) * a.Hkv +
+                            (int64_t)hg * HG) * BLK);
+    const int qpos_ok = (qp >= 0 && qp < a.max_pos) ? qp : -1;
+    if (Lay::QB && first && a.rope && qpos_ok < 0 && g0 + lane < n) report(a.status, KVINJ_ST_BAD_POS);
+    const int qrow0 = rq * a.Hq + hg * HG * Lay::G;  // first q row of the head group
+    int nblk, nhg, nrq, nfirst, nqp;
+    start_lookup(g0 + 32 + lane, nblk, nhg, nrq, nfirst, nqp);
     const int cnt = min(32, n - g0);
     for (int i = 0; i < cnt; ++i) {
       const int r0 = __shfl_sync(0xffffffffu, row0, i);
       const int oki = __shfl_sync(0xffffffffu, ok, i);
+      const int fi = __shfl_sync(0xffffffffu, first, i);
+      const int qri = __shfl_sync(0xffffffffu, qrow0, i);
+      const int qpi = __shfl_sync(0xffffffffu, qpos_ok, i);
       const int gi = g0 + i, st = gi % S;
       int go = 1;
       if (lane == 0) {
+        if (Lay::QB && fi && !flags[0]) {
+          // q rows (and RoPE row) of the piece starting here
+          const int qb = pieces % (Lay::QB ? Lay::QB : 1);
+          uint64_t *qfull = full + 2 * S + qb, *qempty = full + 2 * S + Lay::QB + qb;
+          if (pieces >= Lay::QB &&
+              !mbar_wait_bounded(qempty, (uint32_t)(pieces / Lay::QB - 1) & 1u)) {
+            report(a.status, KVINJ_ST_TIMEOUT);
+            flags[0] = 1;
+          } else {
+            int *qinfo = reinterpret_cast<int *>(sm + Lay::off_qinfo);
+            qinfo[qb] = a.rope ? qpi : -2;
+            const bool trow = a.rope && qpi >= 0;
+            mbar_arrive_expect_tx(qfull, Lay::Q_BYTES + (trow ? Lay::T_BYTES : 0));
+            bulk_load(sm + Lay::off_q + qb * Lay::Q_BYTES, a.q + (int64_t)qri * Lay::D,
+                      Lay::Q_BYTES, qfull);
+            if (trow)
+              bulk_load(sm + Lay::off_t + qb * Lay::T_BYTES, a.rope + (int64_t)qpi * (Lay::D / 2),
+                        Lay::T_BYTES, qfull);
+          }
+          ++pieces;
+        }
         if (flags[0]) {
           go = 0;
         } else if (gi >= S && !mbar_wait_bounded(empty + st, (uint32_t)(gi / S - 1) & 1u)) {
@@ -225,8 +322,8 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
           uint8_t *kd = stages + st * Lay::STAGE_BYTES;
 #pragma unroll
           for (int b = 0; b < NBOX; ++b) {
-            tma_load_2d(kd + b * BOX_BYTES, &tmK, 64 * b, r0, fb);
-            tma_load_2d(kd + Lay::PAGE_BYTES + b * BOX_BYTES, &tmV, 64 * b, r0, fb);
+            tma_load_2d(kd + b * Lay::BOXB, &tmK, 64 * b, r0, fb);
+            tma_load_2d(kd + Lay::UNIT_BYTES + b * Lay::BOXB, &tmV, 64 * b, r0, fb);
           }
         }
       }
@@ -238,60 +335,30 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
       issued = gi + 1;
     }
     blk = nblk;
-    h = nh;
+    hg = nhg;
+    rq = nrq;
+    first = nfirst;
+    qp = nqp;
   }
   if (aborted && lane == 0) {
     // let the copies already in flight land before the CTA can exit
     for (int gi = max(0, issued - S); gi < issued; ++gi)
       mbar_wait_bounded(full + gi % S, (uint32_t)(gi / S) & 1u, 100000000ull);
+    for (int k = max(0, pieces - Lay::QB); k < pieces; ++k)
+      mbar_wait_bounded(full + 2 * S + k % (Lay::QB ? Lay::QB : 1), (uint32_t)(k / (Lay::QB ? Lay::QB : 1)) & 1u,
+                        100000000ull);
   }
 }
 
-// q rows of the G heads of kv group h of request r, rotated at q_pos[r],
-// times scale*log2(e). The lane keeps, for every 64-element box b, the 8
-// elements of chunk `dg`: dims [64b + 8dg, 64b + 8dg + 8).
-template <int D, int G, int DT, int NBOX>
-__device__ __forceinline__ void load_q_rows(const DecodeArgs &a, int r, int h, int dg,
-                                            float (&qr)[G][NBOX][8]) {
-  constexpr int HALF = D / 2;
-  const int qp = a.q_pos[r];
-  const bool rotate = a.rope != nullptr;
-  const bool pos_ok = !rotate || (qp >= 0 && qp < a.max_pos);
-  if (!pos_ok && dg == 0 && (threadIdx.x & 31) == 0) report(a.status, KVINJ_ST_BAD_POS);
-  const float4 *trow = rotate && pos_ok ? a.rope + (int64_t)qp * HALF : nullptr;
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const uint16_t *qrow = a.q + ((int64_t)r * a.Hq + h * G + g) * D;
-#pragma unroll
-    for (int b = 0; b < NBOX; ++b) {
-      const int d0 = 64 * b + 8 * dg;
-      uint4 own = *reinterpret_cast<const uint4 *>(qrow + d0);
-      float x[8];
-      float2 f;
-      f = unpack2<DT>(own.x); x[0] = f.x; x[1] = f.y;
-      f = unpack2<DT>(own.y); x[2] = f.x; x[3] = f.y;
-      f = unpack2<DT>(own.z); x[4] = f.x; x[5] = f.y;
-      f = unpack2<DT>(own.w); x[6] = f.x; x[7] = f.y;
-      if (trow) {
-        const int dp = (d0 + HALF) % D;  // the rotate-half partners
-        uint4 par = *reinterpret_cast<const uint4 *>(qrow + dp);
-        float y[8];
-        f = unpack2<DT>(par.x); y[0] = f.x; y[1] = f.y;
-        f = unpack2<DT>(par.y); y[2] = f.x; y[3] = f.y;
-        f = unpack2<DT>(par.z); y[4] = f.x; y[5] = f.y;
-        f = unpack2<DT>(par.w); y[6] = f.x; y[7] = f.y;
-        const bool first = d0 < HALF;
-        const int f0 = d0 % HALF;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float4 t = __ldg(trow + f0 + e);
-          x[e] = first ? rope_pair(x[e], y[e], t).x : rope_pair(y[e], x[e], t).y;
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qr[g][b][e] = x[e] * a.scale_log2;
-    }
+// wait for unit gi's stage; false (and the abort flag) when the wait gave up
+__device__ __forceinline__ bool consumer_wait(const DecodeArgs &a, uint64_t *full,
+                                              volatile int *flags, int gi, int S) {
+  const bool ok = !flags[0] && mbar_wait_bounded(full + gi % S, (uint32_t)(gi / S) & 1u);
+  if (!ok) {
+    if (!flags[0]) report(a.status, KVINJ_ST_TIMEOUT);
+    flags[0] = 1;
   }
+  return ok;
 }
 
 template <int DT>
@@ -300,81 +367,96 @@ __device__ __forceinline__ uint16_t to16(float x) {
   else return __half_as_ushort(__float2half_rn(x));
 }
 
-// End of a piece: merge the NW per-warp states (already in mm/ml/macc), then
-// either write the output (piece == whole segment) or store this CTA's
-// partial and, if it is the last piece of its segment to arrive, combine all
-// pieces. Called by the NW consumer warps only (named barrier 1).
-template <class Lay, int DT>
-__device__ void finish_piece(const DecodeArgs &a, uint8_t *sm, const CtaRange &rg,
-                             const Piece &pc, int P, int tid) {
-  constexpr int G = Lay::G, D = Lay::D, NW = Lay::NW, NT = NW * 32;
-  volatile int *flags = reinterpret_cast<volatile int *>(sm + Lay::off_flags);
-  const float *mm = reinterpret_cast<const float *>(sm + Lay::off_mm);
-  const float *ml = reinterpret_cast<const float *>(sm + Lay::off_ml);
-  const float *macc = reinterpret_cast<const float *>(sm + Lay::off_macc);
-  named_bar_sync(1, NT);
-  const bool complete = (P == pc.seg_start) && (pc.end == pc.seg_end);
-  uint16_t *orow = a.out + ((int64_t)pc.r * a.Hq + pc.h * G) * D;
-  constexpr int PF = G * (D + 2);  // floats per partial slot: m[G], l[G], acc[G][D]
-  float *mine = a.partials +
-                (size_t)(2 * blockIdx.x + (pc.seg_start <= rg.b0 ? 0 : 1)) * PF;
-  for (int idx = tid; idx < G * D; idx += NT) {
-    const int g = idx / D, d = idx - g * D;
-    float M = -INFINITY;
+// floats of one head's partial state in a workspace slot: m[G], l[G], acc[G][D]
+__host__ __device__ constexpr int partial_floats(int G, int D) { return G * (D + 2); }
+
+// The partial slot of CTA c for the segment starting at unit seg_start:
+// 2c for the first segment in c's range, 2c + 1 for its last one.
+__device__ __forceinline__ float *partial_slot(const DecodeArgs &a, int c, int seg_start,
+                                               const CtaRange &rg, int slot_floats) {
+  return a.partials + (size_t)(2 * c + (seg_start <= range_begin(c, rg) ? 0 : 1)) * slot_floats;
+}
+
+// Combine the partial states of all pieces of a segment into one output row
+// (one query head `g` of kv head `w` of the group), one warp per row: lane j
+// of each round of 32 pieces computes piece j's slot and loads its m and l
+// (the rounds are usually one), the warp reduces the max with shuffles, then
+// every lane accumulates its D/32 dimensions over the pieces, eight pieces'
+// loads in flight at a time.
+template <int D, int G, int HG, int DT>
+__device__ void combine_row(const DecodeArgs &a, const CtaRange &rg, const Piece &pc, int w,
+                            int g, int lane) {
+  constexpr int PF = partial_floats(G, D), SLOT = HG * PF, DPL = D / 32;
+  const int cf = cta_of(pc.seg_start, rg), cl = cta_of(pc.seg_end - 1, rg);
+  const int npc = cl - cf + 1;
+  float A[DPL];
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * G + g]);
-    float Ls = 0.f, A = 0.f;
+  for (int e = 0; e < DPL; ++e) A[e] = 0.f;
+  float M = -INFINITY;  // running max over the rounds
+  float Ls = 0.f;       // lane-partial sum of l * 2^(m - M)
+  for (int c0 = 0; c0 < npc; c0 += 32) {
+    const int cj = cf + c0 + lane;
+    const float *pj = cj <= cl ? partial_slot(a, cj, pc.seg_start, rg, SLOT) + w * PF : nullptr;
+    const float mj = pj ? __ldcg(pj + g) : -INFINITY;
+    const float lj = pj ? __ldcg(pj + G + g) : 0.f;
+    float Mr = mj;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const float mw = mm[w * G + g];
-      const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-      Ls = __fmaf_rn(ml[w * G + g], f, Ls);
-      A = __fmaf_rn(macc[(w * G + g) * D + d], f, A);
-    }
-    if (complete) {
-      orow[idx] = to16<DT>(Ls > 0.f ? A / Ls : 0.f);
-    } else {
-      mine[2 * G + idx] = A;
-      if (d == 0) {
-        mine[g] = M;
-        mine[G + g] = Ls;
+    for (int o = 16; o >= 1; o >>= 1) Mr = fmaxf(Mr, __shfl_xor_sync(0xffffffffu, Mr, o));
+    const float Mn = fmaxf(M, Mr);
+    const float rescale = (M == -INFINITY) ? 0.f : exp2f(M - Mn);  // earlier rounds
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) A[e] *= rescale;
+    Ls *= rescale;
+    M = Mn;
+    const float fj = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
+    Ls = __fmaf_rn(lj, fj, Ls);
+    const int cnt = min(32, npc - c0);
+    for (int j0 = 0; j0 < cnt; j0 += 8) {
+      float v[8][DPL];
+      float f[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = min(j0 + u, cnt - 1);
+        const float *pu = reinterpret_cast<const float *>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(pj), j));
+        f[u] = (j0 + u < cnt) ? __shfl_sync(0xffffffffu, fj, j) : 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) v[u][e] = __ldcg(pu + 2 * G + g * D + lane * DPL + e);
       }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) A[e] = __fmaf_rn(v[u][e], f[u], A[e]);
     }
   }
-  if (!complete) {
-    __threadfence();
-    named_bar_sync(1, NT);
-    const int cf = cta_of(pc.seg_start, rg), cl = cta_of(pc.seg_end - 1, rg);
-    if (tid == 0) {
-      const int old = atomicAdd(a.counters + pc.r * a.Hkv + pc.h, 1);
-      flags[1] = (old == cl - cf) ? 1 : 0;
-    }
-    named_bar_sync(1, NT);
-    if (flags[1]) {
-      __threadfence();
-      for (int idx = tid; idx < G * D; idx += NT) {
-        const int g = idx / D;
-        float M = -INFINITY;
-        for (int c = cf; c <= cl; ++c) {
-          const float *pp = a.partials +
-                            (size_t)(2 * c + (pc.seg_start <= range_begin(c, rg) ? 0 : 1)) * PF;
-          M = fmaxf(M, __ldcg(pp + g));
-        }
-        float Ls = 0.f, A = 0.f;
-        for (int c = cf; c <= cl; ++c) {
-          const float *pp = a.partials +
-                            (size_t)(2 * c + (pc.seg_start <= range_begin(c, rg) ? 0 : 1)) * PF;
-          const float mc = __ldcg(pp + g);
-          const float f = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
-          Ls = __fmaf_rn(__ldcg(pp + G + g), f, Ls);
-          A = __fmaf_rn(__ldcg(pp + 2 * G + idx), f, A);
-        }
-        orow[idx] = to16<DT>(Ls > 0.f ? A / Ls : 0.f);
-      }
-      if (tid == 0) atomicExch(a.counters + pc.r * a.Hkv + pc.h, 0);
-    }
-  }
-  named_bar_sync(1, NT);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+  const int h = pc.hg * HG + w;
+  uint16_t *orow = a.out + ((int64_t)pc.r * a.Hq + (int64_t)h * G + g) * D + lane * DPL;
+#pragma unroll
+  for (int e = 0; e < DPL; e += 2)
+    *reinterpret_cast<uint32_t *>(orow + e) = pack2<DT>(A[e] * inv, A[e + 1] * inv);
+}
+
+// The combine pass: grid (decode CTAs, row groups); block (x, y) combines
+// rows 4y .. 4y+3 (one per warp) of the segment described by decode CTA x.
+constexpr int COMBINE_ROWS = 4;
+template <int D, int G, int HG, int DT>
+__global__ void __launch_bounds__(COMBINE_ROWS * 32) decode_combine_kernel(DecodeArgs a) {
+  const int *d = a.desc + blockIdx.x * DESC_INTS;
+  if (!d[0]) return;
+  const int row = blockIdx.y * COMBINE_ROWS + (threadIdx.x >> 5);
+  if (row >= HG * G) return;
+  Piece pc;
+  pc.r = d[1];
+  pc.hg = d[2];
+  pc.seg_start = d[3];
+  pc.seg_end = d[4];
+  CtaRange rg;
+  rg.n_eff = d[5];
+  rg.Ptot = d[6];
+  combine_row<D, G, HG, DT>(a, rg, pc, row / G, row % G, threadIdx.x & 31);
 }
 
 }  // namespace kvinj

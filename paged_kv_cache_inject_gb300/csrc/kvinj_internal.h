@@ -48,29 +48,33 @@ struct DecodeArgs {
   const float4 *rope;          // nullptr: q already rotated
   int max_pos;
   uint16_t *out;               // [batch][Hq][D]
-  float *partials;             // [2*max_ctas][G][D+2]
-  int *counters;               // [batch*Hkv]
+  float *partials;             // [2*max_ctas][HG][G][D+2]
+  int *desc;                   // [max_ctas][8] cut-segment descriptors
   int32_t *status;
   int batch, Hq, Hkv, max_blocks, layer;
   int64_t num_blocks;
   float scale_log2;            // softmax scale times log2(e)
 };
 
-// decode workspace: counters first, then the partial slots
-size_t decode_partial_floats(int G, int D);  // floats per slot
+// decode workspace: descriptors first, then the partial slots
+size_t decode_partial_floats(int G, int D);  // floats per head of a slot
 int decode_max_ctas();                        // slots/2 the workspace is sized for
-size_t decode_counters_bytes(int batch, int Hkv);
+size_t decode_desc_bytes();
 
 cudaError_t launch_slot_mapping(const int32_t *bt, int max_blocks, int batch, int64_t num_blocks,
                                 int B, const int32_t *seq, const int32_t *pos, int64_t n,
                                 int64_t *out, int32_t *status, cudaStream_t s);
 cudaError_t launch_inject(const InjectArgs &a, int D, int dtype, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs &a, int D, int dtype, cudaStream_t s);
+// HG: kv heads per work unit (a power of two <= 8 dividing Hkv)
+int decode_head_group(int Hkv);
 cudaError_t launch_decode_ffma(const DecodeArgs &a, const CUtensorMap &tmK,
-                               const CUtensorMap &tmV, int D, int G, int dtype, int ctas,
+                               const CUtensorMap &tmV, int D, int G, int HG, int dtype, int ctas,
                                cudaStream_t s);
+cudaError_t launch_decode_mma(const DecodeArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                              int D, int G, int HG, int dtype, int ctas, cudaStream_t s);
 // variant: 1 = CUDA-core FMA kernel, 2 = tensor-core kernel
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                          int D, int G, int dtype, int variant, int ctas, cudaStream_t s);
+                          int D, int G, int HG, int dtype, int variant, int ctas, cudaStream_t s);
 
 }  // namespace kvinj

@@ -115,11 +115,23 @@ class Engine:
                     timer("decode", 1)
         return out
 
+    def capture(self, inp: StepInputs, out: torch.Tensor, timer=None) -> torch.cuda.CUDAGraph:
+        """Capture one step (all its launches) into a CUDA graph. The graph reads
+        the tensors of `inp` and writes `out` in place: refill them, replay."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step(inp, out, timer=timer)
+        return g
+
     def step_from_host(self, host: StepInputs, dev: StepInputs, out: torch.Tensor,
-                       host_out: torch.Tensor):
-        """End to end: pinned host inputs -> device, step, outputs -> pinned host."""
+                       host_out: torch.Tensor, graph: torch.cuda.CUDAGraph | None = None):
+        """End to end: pinned host inputs -> device, step (or its captured graph),
+        outputs -> pinned host."""
         for h, d in zip(host.tensors(), dev.tensors()):
             d.copy_(h, non_blocking=True)
-        self.step(dev, out)
+        if graph is not None:
+            graph.replay()
+        else:
+            self.step(dev, out)
         host_out.copy_(out, non_blocking=True)
         return host_out

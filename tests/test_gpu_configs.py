@@ -53,18 +53,13 @@ def _pool_for(wl, device="cuda"):
     """The full pool when it fits in free memory, else only the drawn chunks
     (same values, remapped ids): the kernels and the bytes they move are the same."""
     import workload.device as gen
+    from workload import stage
     cfg = wl.cfg
     free, _ = torch.cuda.mem_get_info()
     need = cfg.pool_bytes + wl.cache_bytes + (8 << 30)
     if need < free:
         return gen.pool_tensor(wl, device), None
-    ids = np.unique(wl.chunk_ids)
-    t = torch.empty((ids.size, cfg.layers, 2, cfg.chunk_len, cfg.kv_heads, cfg.head_dim),
-                    dtype=gen.torch_dtype(cfg.dtype), device=device)
-    keep = gen.fill_rows(t, ids.astype(np.int64) * cfg.chunk_elems, wl.keys["pool"], cfg.dtype)
-    del keep
-    remap = np.searchsorted(ids, wl.chunk_ids).astype(np.int32)
-    return t, remap
+    return stage.compact_pool(wl, device)
 
 
 @pytest.mark.parametrize("name", W.CONFIG_ORDER)

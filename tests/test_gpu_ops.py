@@ -241,33 +241,40 @@ def _run_decode(kc, vc, q, bt, ctx, q_pos, dt, layer, theta, rope_max, variant=0
 
 
 DECODE_SHAPES = [(64, 1, W.BF16), (64, 2, W.BF16), (128, 4, W.BF16), (128, 8, W.BF16),
-                 (128, 1, W.FP16), (128, 4, W.FP16), (64, 8, W.FP16), (128, 2, W.BF16)]
+                 (128, 1, W.FP16), (128, 4, W.FP16), (64, 8, W.FP16), (128, 2, W.BF16),
+                 (128, 16, W.BF16), (64, 16, W.FP16)]
 
 
+@pytest.mark.parametrize("variant", [1, 2])
 @pytest.mark.parametrize("D,G,dt", DECODE_SHAPES)
 @pytest.mark.parametrize("ctas", [0, 1, 5, 37])
-def test_decode_matches_oracle(D, G, dt, ctas):
+def test_decode_matches_oracle(D, G, dt, ctas, variant):
+    if variant == 1 and G == 16:
+        pytest.skip("the CUDA-core kernel covers G <= 8")
     ctx = [1, 16, 17, 250, 611]
     kc, vc, q, bt = _decode_case(D, G, dt, ctx)
     ctx = np.array(ctx, np.int32)
     q_pos = ctx - 1
     theta = 5e5
     status = status_tensor()
-    got, _ = _run_decode(kc, vc, q, bt, ctx, q_pos, dt, 1, theta, 1000, ctas=ctas, status=status)
+    got, _ = _run_decode(kc, vc, q, bt, ctx, q_pos, dt, 1, theta, 1000, ctas=ctas, status=status,
+                         variant=variant)
     assert status.item() == 0
     want, st = oracle.paged_decode(kc, vc, 1, q, q_pos, bt, ctx, theta, dt)
     assert st == 0
-    assert_decode_close(got, want, f"D{D} G{G} dt{dt} ctas{ctas}")
+    assert_decode_close(got, want, f"D{D} G{G} dt{dt} ctas{ctas} variant{variant}")
 
 
-def test_decode_long_context_and_unrotated_query():
+@pytest.mark.parametrize("variant", [1, 2])
+def test_decode_long_context_and_unrotated_query(variant):
     D, G, dt = 128, 8, W.BF16
     ctx = np.array([9000, 3, 4097], np.int32)
     kc, vc, q, bt = _decode_case(D, G, dt, ctx, Hkv=1, L=1, seed=11)
-    got, _ = _run_decode(kc, vc, q, bt, ctx, ctx - 1, dt, 0, 5e5, 9000)
+    got, _ = _run_decode(kc, vc, q, bt, ctx, ctx - 1, dt, 0, 5e5, 9000, variant=variant)
     want, _ = oracle.paged_decode(kc, vc, 0, q, ctx - 1, bt, ctx, 5e5, dt)
     assert_decode_close(got, want, "long")
-    got, _ = _run_decode(kc, vc, q, bt, ctx, ctx - 1, dt, 0, 5e5, 9000, rotate=False)
+    got, _ = _run_decode(kc, vc, q, bt, ctx, ctx - 1, dt, 0, 5e5, 9000, rotate=False,
+                         variant=variant)
     want, _ = oracle.paged_decode(kc, vc, 0, q, ctx - 1, bt, ctx, 5e5, dt, rotate_q=False)
     assert_decode_close(got, want, "unrotated")
 
@@ -287,18 +294,22 @@ def test_decode_deterministic_and_workspace_reusable():
                              out, ws)
         outs.append(bits(out))
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
-    counters = ws[:4 * 2 * 4].view(torch.int32).cpu().numpy()
-    assert not counters.any(), "split counters must be left at zero"
+    # a workspace needs no initialisation: garbage in it changes nothing
+    ws.fill_(0xAB)
+    out = torch.empty((4, 8, D), dtype=tdt, device="cuda")
+    K.kvinj_paged_decode(cache, rope, 0, from_bits(q, tdt), i32(ctx - 1), i32(bt), i32(ctx), out, ws)
+    assert np.array_equal(bits(out), outs[0])
 
 
-def test_decode_invalid_context_and_block():
+@pytest.mark.parametrize("variant", [1, 2])
+def test_decode_invalid_context_and_block(variant):
     D, G, dt = 64, 2, W.BF16
     ctx_ok = [40, 50, 60]
     kc, vc, q, bt = _decode_case(D, G, dt, ctx_ok, seed=13)
     ctx = np.array([0, 50, 10 ** 6], np.int32)
     status = status_tensor()
     got, _ = _run_decode(kc, vc, q, bt, ctx, np.array([0, 49, 0], np.int32), dt, 0, 1e4, 100,
-                         status=status)
+                         status=status, variant=variant)
     assert status.item() == K.ST_BAD_CTX
     assert not got[0].any() and not got[2].any()
     want, _ = oracle.paged_decode(kc, vc, 0, q[1:2], [49], bt[1:2], [50], 1e4, dt)
@@ -308,7 +319,7 @@ def test_decode_invalid_context_and_block():
     bt2[0, 1] = kc.shape[1] + 5
     status = status_tensor()
     got, _ = _run_decode(kc, vc, q, bt2, np.array(ctx_ok, np.int32), np.array(ctx_ok) - 1, dt, 0,
-                         1e4, 100, status=status)
+                         1e4, 100, status=status, variant=variant)
     assert status.item() == K.ST_BAD_BLOCK
     want, _ = oracle.paged_decode(kc, vc, 0, q[1:], np.array(ctx_ok[1:]) - 1, bt[1:], ctx_ok[1:],
                                   1e4, dt)
@@ -322,3 +333,21 @@ def test_decode_workspace_too_small_is_refused():
         _run_decode(kc, vc, q, bt, np.array([20], np.int32), np.array([19], np.int32), dt, 0, 1e4,
                     40, ws_bytes=64)
     assert e.value.code == K.KVINJ_EWORKSPACE
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("Hkv,G,D", [(4, 4, 128), (8, 4, 128), (12, 2, 64), (16, 1, 128),
+                                     (8, 8, 128)])
+def test_decode_head_groups(Hkv, G, D, variant):
+    # units cover a block of up to 8 kv heads; several groups per block when Hkv > 8
+    dt = W.BF16
+    ctx = [3, 100, 257, 48]
+    kc, vc, q, bt = _decode_case(D, G, dt, ctx, Hkv=Hkv, L=2, seed=21 + Hkv)
+    ctx = np.array(ctx, np.int32)
+    for ctas in (0, 7):
+        status = status_tensor()
+        got, _ = _run_decode(kc, vc, q, bt, ctx, ctx - 1, dt, 1, 5e5, 400, ctas=ctas,
+                             status=status, variant=variant)
+        assert status.item() == 0
+        want, _ = oracle.paged_decode(kc, vc, 1, q, ctx - 1, bt, ctx, 5e5, dt)
+        assert_decode_close(got, want, f"Hkv{Hkv} G{G} D{D} ctas{ctas} variant{variant}")

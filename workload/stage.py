@@ -26,6 +26,20 @@ def make_engine(wl: Workload, device="cuda", pool: torch.Tensor | None = None) -
                   max_pos=wl.max_pos, theta=cfg.theta, batch=cfg.batch, pool=pool, device=device)
 
 
+def compact_pool(wl: Workload, device="cuda"):
+    """Only the chunks this batch draws, with their values (same bits as the
+    full pool): returns (pool tensor, remapped chunk ids int32). The kernels
+    and the bytes they move are those of the full pool; only capacity differs."""
+    cfg = wl.cfg
+    ids = np.unique(wl.chunk_ids)
+    t = torch.empty((ids.size, cfg.layers, 2, cfg.chunk_len, cfg.kv_heads, cfg.head_dim),
+                    dtype=gen.torch_dtype(cfg.dtype), device=device)
+    keep = gen.fill_rows(t, ids.astype(np.int64) * cfg.chunk_elems, wl.keys["pool"], cfg.dtype)
+    torch.cuda.synchronize()
+    del keep
+    return t, np.searchsorted(ids, wl.chunk_ids).astype(np.int32)
+
+
 def _i32(a, device):
     return torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(device)
 
