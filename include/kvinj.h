@@ -196,6 +196,28 @@ int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int3
                           void *workspace, size_t ws_bytes, int32_t *dev_status,
                           kvinj_stream_t stream, int32_t variant, int32_t ctas);
 
+/* Paged decode without a caller-provided workspace (no counterpart in the
+ * pages; an addition of this library). For callers that cannot allocate
+ * device memory where they run -- an engine hook or plugin that must not call
+ * cudaMalloc (it can implicitly synchronize the device), a process whose
+ * memory is already handed out, a path that must not fail on memory
+ * pressure mid-request. Same arguments and results as kvinj_paged_decode;
+ * the scratch is a fixed device array of KVINJ_STATIC_SCRATCH_BYTES that
+ * every GPU loading this library holds until exit. Nothing is allocated or
+ * freed. Returns KVINJ_EWORKSPACE when this shape needs more scratch than
+ * that (kvinj_decode_workspace_size() > KVINJ_STATIC_SCRATCH_BYTES; enough
+ * for D = 128 with up to 64 query heads per head group on a 152-SM GPU).
+ * The first call on a device looks up the array's address (make it before
+ * any stream capture). All calls on a device share the array and leave their
+ * contents in it; nothing in it needs to start at zero, but calls whose
+ * kernels overlap on the GPU race on it. */
+#define KVINJ_STATIC_SCRATCH_BYTES (24u << 20)
+int kvinj_paged_decode_static(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                              int32_t num_q_heads, const void *q, const int32_t *q_pos,
+                              const int32_t *block_tables, int32_t max_blocks,
+                              const int32_t *context_lens, int32_t batch, float scale, void *out,
+                              int32_t *dev_status, kvinj_stream_t stream);
+
 /* KV bytes of `tokens` tokens: 2 * layers * heads * head_dim * tokens *
  * bytes_per_elem ("LLM Inference: KV Caching", What the cache costs). */
 int64_t kvinj_kv_bytes(int32_t layers, int32_t heads, int32_t head_dim, int64_t tokens,

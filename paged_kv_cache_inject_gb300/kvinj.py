@@ -27,7 +27,8 @@ ST_BAD_CTX, ST_BAD_SEQ, ST_TIMEOUT = 0x10, 0x20, 0x40
 EXPORTS = [
     "kvinj_rope_table_bytes", "kvinj_rope_table_host", "kvinj_slot_mapping", "kvinj_inject",
     "kvinj_append", "kvinj_decode_workspace_size", "kvinj_decode_workspace_init",
-    "kvinj_paged_decode", "kvinj_paged_decode_ex", "kvinj_kv_bytes", "kvinj_strerror",
+    "kvinj_paged_decode", "kvinj_paged_decode_ex", "kvinj_paged_decode_static", "kvinj_kv_bytes",
+    "kvinj_strerror",
 ]
 
 
@@ -83,6 +84,8 @@ def load(path: str = LIB_PATH):
                                                   ctypes.c_float, P, P, sz, P, P]),
             "kvinj_paged_decode_ex": (ctypes.c_int, [P, P, i32, i32, P, P, P, i32, P, i32,
                                                      ctypes.c_float, P, P, sz, P, P, i32, i32]),
+            "kvinj_paged_decode_static": (ctypes.c_int, [P, P, i32, i32, P, P, P, i32, P, i32,
+                                                         ctypes.c_float, P, P, P]),
             "kvinj_kv_bytes": (i64, [i32, i32, i32, i64, i32]),
             "kvinj_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         }
@@ -255,6 +258,20 @@ def kvinj_paged_decode(cache: Cache, rope: Rope | None, layer: int, q, q_pos, bl
                                      float(scale), _ptr(out), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(),
                                      _ptr(status), _stream(stream)))
+    return out
+
+
+def kvinj_paged_decode_static(cache: Cache, rope: Rope | None, layer: int, q, q_pos,
+                              block_tables, context_lens, out, scale: float = 0.0, status=None,
+                              stream=None):
+    """kvinj_paged_decode with the library's fixed device scratch (no workspace)."""
+    batch, Hq, _ = q.shape
+    _check("kvinj_paged_decode_static",
+           load().kvinj_paged_decode_static(cache.ref, rope.ref if rope is not None else None,
+                                            layer, Hq, _ptr(q), _ptr(q_pos), _ptr(block_tables),
+                                            block_tables.shape[1], _ptr(context_lens), batch,
+                                            float(scale), _ptr(out), _ptr(status),
+                                            _stream(stream)))
     return out
 
 
