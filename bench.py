@@ -442,7 +442,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG)
-    ap.add_argument("--variant", type=int, default=0, help="decode kernel: 0 auto, 1 FMA, 2 mma")
+    ap.add_argument("--variant", type=int, default=0, help="decode kernel: 0 auto, 1 FMA, 2 mma.sync, 3 tcgen05")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly from Python")
     ap.add_argument("--layers", type=int, default=0,

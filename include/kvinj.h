@@ -154,13 +154,15 @@ int kvinj_append(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer
                  kvinj_stream_t stream);
 
 /* Workspace bytes kvinj_paged_decode needs for this shape on the current
- * device (partial softmax states of the split-K pieces plus one counter per
- * (request, kv head)). */
+ * device: one descriptor per CTA of the split-K grid (the segment it closes)
+ * and two partial softmax states (m, l and the unnormalised output of every
+ * query head of a head group) per CTA. */
 size_t kvinj_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim);
 
-/* Zero a decode workspace (its counters must start at zero; every decode call
- * leaves them at zero again). Call once after allocating it. */
+/* Zero a decode workspace. Optional: every decode call writes each
+ * descriptor and partial state before reading it, so the workspace may hold
+ * anything; zeroing only makes its contents deterministic for inspection. */
 int kvinj_decode_workspace_init(void *workspace, size_t ws_bytes, kvinj_stream_t stream);
 
 /* Paged decode attention ("LLM Inference: KV Caching", attention and Paged
@@ -172,11 +174,14 @@ int kvinj_decode_workspace_init(void *workspace, size_t ws_bytes, kvinj_stream_t
  *   out[r][qh] = sum_p softmax_p(scale * q'.K_p) V_p
  * scale <= 0 means 1/sqrt(D). q, out: device [batch][Hq][D] in the cache
  * dtype; accumulation is fp32. workspace: device, at least
- * kvinj_decode_workspace_size() bytes, zeroed once by
- * kvinj_decode_workspace_init(); calls sharing one workspace must not overlap
- * in time. A request with an invalid context gets a zero output and
- * KVINJ_ST_BAD_CTX. Requires block_size 16, D 64 or 128, Hq % Hkv == 0,
- * Hq/Hkv <= 16 and batch <= 4096 (KVINJ_EUNSUPPORTED otherwise). */
+ * kvinj_decode_workspace_size() bytes, any contents; calls sharing one
+ * workspace must not overlap in time. A request with an invalid context gets
+ * a zero output and KVINJ_ST_BAD_CTX; a block-table entry out of range is
+ * treated as a block of masked tokens (KVINJ_ST_BAD_BLOCK); a q position out
+ * of the RoPE table leaves q unrotated (KVINJ_ST_BAD_POS). Requires
+ * block_size 16, D 64 or 128, Hq % Hkv == 0, Hq/Hkv <= 16 and batch <= 4096
+ * (KVINJ_EUNSUPPORTED otherwise). Launches two kernels on `stream`: the
+ * split-K pass and the combine of the segments it cut. */
 int kvinj_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
                        int32_t num_q_heads, const void *q, const int32_t *q_pos,
                        const int32_t *block_tables, int32_t max_blocks,
@@ -184,11 +189,15 @@ int kvinj_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t
                        void *workspace, size_t ws_bytes, int32_t *dev_status,
                        kvinj_stream_t stream);
 
-/* Same as kvinj_paged_decode with an explicit kernel choice:
- * variant 0 = automatic, 1 = CUDA-core FMA kernel (G in {1, 2, 4, 8}),
- * 2 = tensor-core mma.sync kernel (G in {1, 2, 4, 8, 16}). `ctas` > 0
- * overrides the grid size (1 .. 2 x the SM count, the workspace slots);
- * 0 = one CTA per SM. */
+/* Same as kvinj_paged_decode with an explicit kernel choice (G = Hq/Hkv):
+ * variant 0 = automatic (3 where it applies, else 2 for G >= 4, else 1),
+ * 1 = CUDA-core FMA kernel (G in {1, 2, 4, 8}),
+ * 2 = warp-level mma.sync kernel (G in {1, 2, 4, 8, 16}),
+ * 3 = tcgen05 kernel, accumulators in tensor memory (D = 128, Hkv a multiple
+ *     of 8, G in {1, 2, 4, 8}).
+ * KVINJ_EUNSUPPORTED when the chosen variant does not cover the shape.
+ * `ctas` > 0 overrides the grid size (1 .. 2 x the SM count, the workspace
+ * slots); 0 = one CTA per SM. */
 int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
                           int32_t num_q_heads, const void *q, const int32_t *q_pos,
                           const int32_t *block_tables, int32_t max_blocks,

@@ -250,10 +250,13 @@ int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int3
   if (!q || !block_tables || !context_lens || !out || !workspace) return KVINJ_EINVAL;
   if (rope && !q_pos) return KVINJ_EINVAL;
   if (!aligned16(q) || !aligned16(out)) return KVINJ_EINVAL;
-  if (variant < 0 || variant > 2) return KVINJ_EINVAL;
-  if (variant == 0) variant = G >= 4 ? 2 : 1;
-  if (variant == 1 && !(G == 1 || G == 2 || G == 4 || G == 8)) return KVINJ_EUNSUPPORTED;
-  if (variant == 2 && !(G == 1 || G == 2 || G == 4 || G == 8 || G == 16)) return KVINJ_EUNSUPPORTED;
+  if (variant < 0 || variant > 3) return KVINJ_EINVAL;
+  const bool g_pow2_8 = G == 1 || G == 2 || G == 4 || G == 8;
+  const bool umma_ok = D == 128 && decode_head_group(Hkv) == 8 && g_pow2_8;
+  if (variant == 0) variant = umma_ok ? 3 : (G >= 4 ? 2 : 1);
+  if (variant == 1 && !g_pow2_8) return KVINJ_EUNSUPPORTED;
+  if (variant == 2 && !(g_pow2_8 || G == 16)) return KVINJ_EUNSUPPORTED;
+  if (variant == 3 && !umma_ok) return KVINJ_EUNSUPPORTED;
   if ((int64_t)batch * Hkv * max_blocks >= (int64_t)1 << 31) return KVINJ_EUNSUPPORTED;
   if (batch > 4096) return KVINJ_EUNSUPPORTED;  // per-request prefix sums live in shared memory
   if ((int64_t)cache->num_layers * cache->num_blocks * Hkv * 16 >= (int64_t)1 << 31)
@@ -325,6 +328,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tmK, const CUt
                           int D, int G, int HG, int dtype, int variant, int ctas, cudaStream_t s) {
   if (variant == 1) return launch_decode_ffma(a, tmK, tmV, D, G, HG, dtype, ctas, s);
   if (variant == 2) return launch_decode_mma(a, tmK, tmV, D, G, HG, dtype, ctas, s);
+  if (variant == 3) return launch_decode_umma(a, tmK, tmV, D, G, HG, dtype, ctas, s);
   return cudaErrorInvalidValue;
 }
 }  // namespace kvinj

@@ -38,6 +38,8 @@ template <int D_, int G_, int HG_, int S_, int QB_ = 0>
 struct DecodeLayout {
   static constexpr int D = D_, G = G_, HG = HG_, S = S_;
   static constexpr int QB = QB_;                        // q staging buffers (0 = none)
+  static constexpr int EMPTY_ARRIVALS = HG;             // consumer warps free a stage
+  static constexpr bool QPOS_SM = false;  // q positions copied to shared memory after pre[]
   static constexpr int NBOX = D / 64;                   // 64-element (128-byte) column boxes
   static constexpr int BOXB = HG * BLK * 128;           // bytes of one box: HG*16 rows
   static constexpr int UNIT_BYTES = NBOX * BOXB;        // K (or V) of one unit
@@ -152,6 +154,8 @@ __device__ __forceinline__ int valid_pages(const DecodeArgs &a, int r) {
 // invalid. Returns false when this CTA has no units.
 template <class Lay, int NT>
 __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) {
+  // the combine pass may launch now: it waits for this grid's completion
+  griddep_launch_dependents();
   int *pre = reinterpret_cast<int *>(sm + Lay::off_pre);
   int *flags = reinterpret_cast<int *>(sm + Lay::off_flags);
   int *ws = flags + 8;
@@ -163,6 +167,8 @@ __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) 
     const int r = base + tid;
     int v = 0;
     if (r < a.batch) {
+      if constexpr (Lay::QPOS_SM)
+        reinterpret_cast<int *>(sm + Lay::off_pre)[a.batch + 1 + r] = a.rope ? a.q_pos[r] : -1;
       v = valid_pages(a, r) * ngrp;
       if (v == 0 && blockIdx.x == 0) {
         uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t)r * a.Hq * Lay::D);
@@ -208,7 +214,7 @@ __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) 
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + Lay::off_bar);
     for (int s = 0; s < Lay::S; ++s) {
       mbar_init(full + s, 1);                 // the producer's arrive + the TMA bytes
-      mbar_init(full + Lay::S + s, Lay::HG);  // every consumer warp releases
+      mbar_init(full + Lay::S + s, Lay::EMPTY_ARRIVALS);  // the consumers' releases
     }
     for (int b = 0; b < Lay::QB; ++b) {
       mbar_init(full + 2 * Lay::S + b, 1);
@@ -289,10 +295,11 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
       if (lane == 0) {
         if (Lay::QB && fi && !flags[0]) {
           // q rows (and RoPE row) of the piece starting here
-          const int qb = pieces % (Lay::QB ? Lay::QB : 1);
+          constexpr int QBD = Lay::QB ? Lay::QB : 1;
+          const int qb = pieces % QBD;
           uint64_t *qfull = full + 2 * S + qb, *qempty = full + 2 * S + Lay::QB + qb;
           if (pieces >= Lay::QB &&
-              !mbar_wait_bounded(qempty, (uint32_t)(pieces / Lay::QB - 1) & 1u)) {
+              !mbar_wait_bounded(qempty, (uint32_t)(pieces / QBD - 1) & 1u)) {
             report(a.status, KVINJ_ST_TIMEOUT);
             flags[0] = 1;
           } else {
@@ -444,6 +451,7 @@ __device__ void combine_row(const DecodeArgs &a, const CtaRange &rg, const Piece
 constexpr int COMBINE_ROWS = 4;
 template <int D, int G, int HG, int DT>
 __global__ void __launch_bounds__(COMBINE_ROWS * 32) decode_combine_kernel(DecodeArgs a) {
+  griddep_wait();  // the split-K pass complete, its partials and descriptors visible
   const int *d = a.desc + blockIdx.x * DESC_INTS;
   if (!d[0]) return;
   const int row = blockIdx.y * COMBINE_ROWS + (threadIdx.x >> 5);
@@ -457,6 +465,24 @@ __global__ void __launch_bounds__(COMBINE_ROWS * 32) decode_combine_kernel(Decod
   rg.n_eff = d[5];
   rg.Ptot = d[6];
   combine_row<D, G, HG, DT>(a, rg, pc, row / G, row % G, threadIdx.x & 31);
+}
+
+// Launch the combine pass for a split-K grid of `ctas` CTAs on stream s, as a
+// programmatic dependent of the kernel launched just before it: its CTAs may
+// be scheduled while that kernel runs and wait for it in griddep_wait.
+template <int D, int G, int HG, int DT>
+cudaError_t launch_combine(const DecodeArgs &a, int ctas, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas, (HG * G + COMBINE_ROWS - 1) / COMBINE_ROWS);
+  cfg.blockDim = dim3(COMBINE_ROWS * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, G, HG, DT>, a);
 }
 
 }  // namespace kvinj

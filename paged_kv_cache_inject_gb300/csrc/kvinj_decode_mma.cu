@@ -404,9 +404,9 @@ static cudaError_t launch_mma(const DecodeArgs &a, const CUtensorMap &tmK, const
     attr_set = true;
   }
   kern<<<ctas, (HG + 1) * 32, smem, s>>>(tmK, tmV, a);
-  decode_combine_kernel<D, G, HG, DT>
-      <<<dim3(ctas, (HG * G + COMBINE_ROWS - 1) / COMBINE_ROWS), COMBINE_ROWS * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_combine<D, G, HG, DT>(a, ctas, s);
 }
 
 cudaError_t launch_decode_mma(const DecodeArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmV,

@@ -73,7 +73,11 @@ cudaError_t launch_decode_ffma(const DecodeArgs &a, const CUtensorMap &tmK,
                                cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmV,
                               int D, int G, int HG, int dtype, int ctas, cudaStream_t s);
-// variant: 1 = CUDA-core FMA kernel, 2 = tensor-core kernel
+// tcgen05 kernel: D = 128, HG = 8, G in {1, 2, 4, 8}
+cudaError_t launch_decode_umma(const DecodeArgs &a, const CUtensorMap &tmK,
+                               const CUtensorMap &tmV, int D, int G, int HG, int dtype, int ctas,
+                               cudaStream_t s);
+// variant: 1 = CUDA-core FMA kernel, 2 = mma.sync kernel, 3 = tcgen05 kernel
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmV,
                           int D, int G, int HG, int dtype, int variant, int ctas, cudaStream_t s);
 

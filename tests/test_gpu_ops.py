@@ -224,7 +224,7 @@ def _decode_case(D, G, dt, ctx, Hkv=2, L=2, seed=7, spare=3):
 
 
 def _run_decode(kc, vc, q, bt, ctx, q_pos, dt, layer, theta, rope_max, variant=0, ctas=0,
-                rotate=True, ws_bytes=None, status=None):
+                rotate=True, ws_bytes=None, status=None, scale=0.0):
     tdt = torch_dtype(dt)
     D = kc.shape[-1]
     cache = K.Cache(from_bits(kc, tdt), from_bits(vc, tdt))
@@ -235,7 +235,7 @@ def _run_decode(kc, vc, q, bt, ctx, q_pos, dt, layer, theta, rope_max, variant=0
     ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
     out = torch.full((batch, Hq, D), float("nan"), dtype=tdt, device="cuda")
     K.kvinj_paged_decode_ex(cache, rope, layer, from_bits(q, tdt), i32(q_pos), i32(bt), i32(ctx),
-                            out, ws, 0.0, status, None, variant, ctas)
+                            out, ws, scale, status, None, variant, ctas)
     torch.cuda.synchronize()
     return out.float().cpu().numpy().astype(np.float64), ws
 
@@ -335,11 +335,17 @@ def test_decode_workspace_too_small_is_refused():
     assert e.value.code == K.KVINJ_EWORKSPACE
 
 
-@pytest.mark.parametrize("variant", [1, 2])
+def _umma_covers(D, G, Hkv):
+    return D == 128 and Hkv % 8 == 0 and G in (1, 2, 4, 8)
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3])
 @pytest.mark.parametrize("Hkv,G,D", [(4, 4, 128), (8, 4, 128), (12, 2, 64), (16, 1, 128),
                                      (8, 8, 128)])
 def test_decode_head_groups(Hkv, G, D, variant):
     # units cover a block of up to 8 kv heads; several groups per block when Hkv > 8
+    if variant == 3 and not _umma_covers(D, G, Hkv):
+        pytest.skip("the tcgen05 kernel needs D = 128 and groups of 8 kv heads")
     dt = W.BF16
     ctx = [3, 100, 257, 48]
     kc, vc, q, bt = _decode_case(D, G, dt, ctx, Hkv=Hkv, L=2, seed=21 + Hkv)
@@ -351,3 +357,96 @@ def test_decode_head_groups(Hkv, G, D, variant):
         assert status.item() == 0
         want, _ = oracle.paged_decode(kc, vc, 1, q, ctx - 1, bt, ctx, 5e5, dt)
         assert_decode_close(got, want, f"Hkv{Hkv} G{G} D{D} ctas{ctas} variant{variant}")
+
+
+# ---------------------------------------------------------------------------
+# tcgen05 decode (variant 3): D = 128, head groups of 8 kv heads
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("dt", [W.BF16, W.FP16])
+@pytest.mark.parametrize("Hkv", [8, 16])
+@pytest.mark.parametrize("ctas", [0, 1, 5, 37])
+def test_decode_umma_matches_oracle(G, dt, Hkv, ctas):
+    ctx = [1, 16, 17, 250, 611]
+    kc, vc, q, bt = _decode_case(128, G, dt, ctx, Hkv=Hkv, seed=40 + G + Hkv)
+    ctx = np.array(ctx, np.int32)
+    status = status_tensor()
+    got, _ = _run_decode(kc, vc, q, bt, ctx, ctx - 1, dt, 1, 5e5, 1000, ctas=ctas, status=status,
+                         variant=3)
+    assert status.item() == 0
+    want, st = oracle.paged_decode(kc, vc, 1, q, ctx - 1, bt, ctx, 5e5, dt)
+    assert st == 0
+    assert_decode_close(got, want, f"umma G{G} dt{dt} Hkv{Hkv} ctas{ctas}")
+
+
+@pytest.mark.parametrize("scale", [0.0, 0.5, 3.0])
+@pytest.mark.parametrize("G", [4, 8])
+def test_decode_umma_large_logits_move_the_maximum(scale, G):
+    # with large logit scales the per-head maximum jumps by far more than the
+    # lazy-rescale threshold from unit to unit: exercises the O / l rescaling
+    dt = W.BF16
+    ctx = np.array([2000, 517, 64, 1300], np.int32)
+    kc, vc, q, bt = _decode_case(128, G, dt, ctx, Hkv=8, L=1, seed=50 + G)
+    for ctas in (0, 3):
+        status = status_tensor()
+        got, _ = _run_decode(kc, vc, q, bt, ctx, ctx - 1, dt, 0, 5e5, 2100, ctas=ctas,
+                             status=status, variant=3, scale=scale)
+        assert status.item() == 0
+        want, _ = oracle.paged_decode(kc, vc, 0, q, ctx - 1, bt, ctx, 5e5, dt, scale=scale)
+        assert_decode_close(got, want, f"umma scale{scale} G{G} ctas{ctas}")
+
+
+def test_decode_umma_long_context_unrotated_and_bad_inputs():
+    D, G, dt = 128, 4, W.BF16
+    ctx = np.array([9000, 3, 4097], np.int32)
+    kc, vc, q, bt = _decode_case(D, G, dt, ctx, Hkv=8, L=1, seed=61)
+    got, _ = _run_decode(kc, vc, q, bt, ctx, ctx - 1, dt, 0, 5e5, 9000, variant=3)
+    want, _ = oracle.paged_decode(kc, vc, 0, q, ctx - 1, bt, ctx, 5e5, dt)
+    assert_decode_close(got, want, "umma long")
+    got, _ = _run_decode(kc, vc, q, bt, ctx, ctx - 1, dt, 0, 5e5, 9000, rotate=False, variant=3)
+    want, _ = oracle.paged_decode(kc, vc, 0, q, ctx - 1, bt, ctx, 5e5, dt, rotate_q=False)
+    assert_decode_close(got, want, "umma unrotated")
+    # invalid context lengths: zero output and a status bit, neighbours intact
+    bad = np.array([0, 3, 10 ** 6], np.int32)
+    status = status_tensor()
+    got, _ = _run_decode(kc, vc, q, bt, bad, np.array([0, 2, 0], np.int32), dt, 0, 5e5, 9000,
+                         status=status, variant=3)
+    assert status.item() == K.ST_BAD_CTX
+    assert not got[0].any() and not got[2].any()
+    want, _ = oracle.paged_decode(kc, vc, 0, q[1:2], [2], bt[1:2], [3], 5e5, dt)
+    assert_decode_close(got[1:2], want, "umma valid request next to invalid ones")
+    bt2 = bt.copy()
+    bt2[0, 5] = kc.shape[1] + 7  # a block-table entry outside the cache
+    status = status_tensor()
+    got, _ = _run_decode(kc, vc, q, bt2, ctx, ctx - 1, dt, 0, 5e5, 9000, status=status, variant=3)
+    assert status.item() == K.ST_BAD_BLOCK
+    want, _ = oracle.paged_decode(kc, vc, 0, q[1:], ctx[1:] - 1, bt[1:], ctx[1:], 5e5, dt)
+    assert_decode_close(got[1:], want, "umma requests after a bad block")
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3])
+def test_decode_ignores_nan_rows_past_the_context(variant):
+    # rows of a request's last block past its context may hold anything; NaN
+    # bit patterns there must not reach the output
+    D, G, dt, Hkv = 128, 4, W.BF16, 8
+    ctx = np.array([33, 250, 7, 16], np.int32)
+    kc, vc, q, bt = _decode_case(D, G, dt, ctx, Hkv=Hkv, L=2, seed=71)
+    for r, c in enumerate(ctx):
+        if c % 16:
+            blk = bt[r, c // 16]
+            kc[1, blk, :, c % 16:, :] = 0x7FC0
+            vc[1, blk, :, c % 16:, :] = 0xFFC1
+    got, _ = _run_decode(kc, vc, q, bt, ctx, ctx - 1, dt, 1, 5e5, 300, variant=variant)
+    assert np.isfinite(got).all()
+    want, _ = oracle.paged_decode(kc, vc, 1, q, ctx - 1, bt, ctx, 5e5, dt)
+    assert_decode_close(got, want, f"nan tail variant{variant}")
+
+
+def test_decode_umma_refuses_shapes_it_does_not_cover():
+    dt = W.BF16
+    for D, G, Hkv in [(64, 4, 8), (128, 4, 4), (128, 16, 8)]:
+        kc, vc, q, bt = _decode_case(D, G, dt, [20], Hkv=Hkv, seed=81)
+        with pytest.raises(K.KvinjError) as e:
+            _run_decode(kc, vc, q, bt, np.array([20], np.int32), np.array([19], np.int32), dt, 0,
+                        1e4, 40, variant=3)
+        assert e.value.code == K.KVINJ_EUNSUPPORTED
