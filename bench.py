@@ -291,45 +291,29 @@ def run_gpu(args):
     if eng.status.item() != 0:
         raise RuntimeError(f"device status {eng.status.item():#x} after warm-up")
 
-    # One CUDA graph per timed step (the decode loop is launch-bound from
-    # Python otherwise), each with its own timing events around the inject
-    # and decode launches, recorded as graph nodes on the launching stream.
-    def make_timer(store, external):
-        pending = {}
+    # The timed region replays one CUDA graph of the whole step (the decode
+    # loop is launch-bound from Python otherwise); nothing but the step's own
+    # kernels is inside it. Per-kernel times come from separate graphs of the
+    # same launches (inject alone; the L decode launches alone), timed with
+    # events around their replays on the launching stream.
+    use_graph = not args.no_graph
+    g_step = eng.capture(inp, out) if use_graph else None
 
-        def timer(kind, which):
-            e = torch.cuda.Event(enable_timing=True, external=external)
-            e.record()
-            if which == 0:
-                pending[kind] = e
-            else:
-                store[kind].append((pending.pop(kind), e))
-        return timer
+    def run_step():
+        if g_step is not None:
+            g_step.replay()
+        else:
+            eng.step(inp, out)
 
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-        external_ok = not args.no_graph
-    except TypeError:
-        external_ok = False
-    graphs, stores = [], []
-    if external_ok:
-        for _ in range(args.steps):
-            store = {"inject": [], "decode": []}
-            graphs.append(eng.capture(inp, out, timer=make_timer(store, True)))
-            stores.append(store)
-        for _ in range(args.warmup):
-            graphs[0].replay()
+    for _ in range(args.warmup):
+        run_step()
     barrier()
-    eager_store = {"inject": [], "decode": []}
     with ClockSampler(local) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for k in range(args.steps):
-            if external_ok:
-                graphs[k].replay()
-            else:
-                eng.step(inp, out, timer=make_timer(eager_store, False))
+            run_step()
         t_end.record(stream)
         barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
@@ -339,28 +323,56 @@ def run_gpu(args):
         elapsed_ms = float(t.item())
     ms_step = elapsed_ms / args.steps
     value = ws * nbytes["total"] / (ms_step * 1e-3) / 1e9
-    ev = {"inject": [], "decode": []}
-    for st in (stores if external_ok else [eager_store]):
-        for kind in ev:
-            ev[kind].extend(st[kind])
 
-    dec_ms = [a.elapsed_time(b) for a, b in ev["decode"]]
-    inj_ms = [a.elapsed_time(b) for a, b in ev["inject"]]
-    dec_avg = sum(dec_ms) / len(dec_ms)
-    inj_avg = sum(inj_ms) / len(inj_ms)
+    # per-kernel timing: inject (all layers, one launch) and decode (one
+    # launch pair -- split-K pass + combine -- per layer)
+    slots = eng.slot_mapping(inp.block_tables, inp.map_seq, inp.map_pos)
+    n_inj_tok = inp.chunk_ids.numel() * eng.chunk_len
+
+    def inject_only():
+        eng.inject(inp.chunk_ids, inp.start_pos, slots[:n_inj_tok])
+
+    def decode_only():
+        for s in range(cfg.steps):
+            for layer in range(cfg.layers):
+                eng.decode(layer, inp.q[s, layer], inp.q_pos[s], inp.block_tables,
+                           inp.ctx_lens[s], out[s, layer])
+
+    def part_ms(fn, reps):
+        g = None
+        if use_graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+        run = g.replay if g is not None else fn
+        for _ in range(2):
+            run()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    inj_avg = part_ms(inject_only, max(3, args.steps))
+    dec_avg = part_ms(decode_only, max(3, args.steps)) / (cfg.layers * cfg.steps)
     per_launch_decode = nbytes["decode"] / (cfg.layers * cfg.steps)
     dec_gbs = per_launch_decode / (dec_avg * 1e-3) / 1e9
     inj_gbs = nbytes["inject"] / (inj_avg * 1e-3) / 1e9
     inj_tok_s = wl.n_inj * cfg.chunk_len / (inj_avg * 1e-3)
     peak, peak_kind = _peaks()
-    launches_per_step = 2 + 2 * cfg.layers * cfg.steps
+    # slot mapping + inject, then per step and layer: append, split-K decode, combine
+    launches_per_step = 2 + 3 * cfg.layers * cfg.steps
 
     # end to end through host buffers (pinned), same metric
     e2e = None
     if not args.no_e2e:
         host = stage.pinned_copy(inp)
         host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        g0 = graphs[0] if graphs else None
+        g0 = g_step
         for _ in range(max(1, args.warmup)):
             eng.step_from_host(host, inp, out, host_out, g0)
         barrier()
@@ -408,7 +420,7 @@ def run_gpu(args):
                    "l2": (f"inputs larger than L2: {nbytes['total'] / 1e9:.2f} GB touched per "
                           f"step; no flush"),
                    "decode_variant": args.variant,
-                   "launch": "cuda graph per step" if external_ok else "eager",
+                   "launch": "cuda graph per step" if use_graph else "eager",
                    "pool": ("drawn chunks only" if args.compact_pool else
                             f"full, {cfg.pool_bytes / 1e9:.1f} GB resident")},
         "parts": {

@@ -298,8 +298,7 @@ static cudaError_t launch_ffma(const DecodeArgs &a, const CUtensorMap &tmK,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<ctas, (HG + 1) * 32, smem, s>>>(tmK, tmV, a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(kern, dim3(ctas), dim3((HG + 1) * 32), smem, s, tmK, tmV, a);
   if (e != cudaSuccess) return e;
   return launch_combine<D, G, HG, DT>(a, ctas, s);
 }

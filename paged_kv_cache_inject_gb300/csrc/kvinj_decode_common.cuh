@@ -144,16 +144,14 @@ __device__ __forceinline__ void write_descriptor(const DecodeArgs &a, const int 
   d[6] = rg->Ptot;
 }
 
-__device__ __forceinline__ int valid_pages(const DecodeArgs &a, int r) {
-  const int c = a.context_lens[r];
-  return (c > 0 && c <= a.max_blocks * BLK) ? (c + BLK - 1) / BLK : 0;
-}
-
 // Units per request -> prefix sums pre[0..batch], this CTA's range, barrier
 // set-up. CTA 0 also zeroes the output of requests whose context length is
 // invalid. Returns false when this CTA has no units.
 template <class Lay, int NT>
 __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) {
+  // launched as a programmatic dependent: every input may come from the
+  // kernel before this one, so nothing is read before it has completed
+  griddep_wait();
   // the combine pass may launch now: it waits for this grid's completion
   griddep_launch_dependents();
   int *pre = reinterpret_cast<int *>(sm + Lay::off_pre);
@@ -167,9 +165,11 @@ __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) 
     const int r = base + tid;
     int v = 0;
     if (r < a.batch) {
-      if constexpr (Lay::QPOS_SM)
-        reinterpret_cast<int *>(sm + Lay::off_pre)[a.batch + 1 + r] = a.rope ? a.q_pos[r] : -1;
-      v = valid_pages(a, r) * ngrp;
+      // both loads in flight together, before any shared-memory store
+      const int qp = (Lay::QPOS_SM && a.rope) ? __ldg(a.q_pos + r) : -1;
+      const int c = __ldg(a.context_lens + r);
+      if constexpr (Lay::QPOS_SM) reinterpret_cast<int *>(sm + Lay::off_pre)[a.batch + 1 + r] = qp;
+      v = ((c > 0 && c <= a.max_blocks * BLK) ? (c + BLK - 1) / BLK : 0) * ngrp;
       if (v == 0 && blockIdx.x == 0) {
         uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t)r * a.Hq * Lay::D);
         for (int i = 0; i < a.Hq * Lay::D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
@@ -384,78 +384,88 @@ __device__ __forceinline__ float *partial_slot(const DecodeArgs &a, int c, int s
   return a.partials + (size_t)(2 * c + (seg_start <= range_begin(c, rg) ? 0 : 1)) * slot_floats;
 }
 
-// Combine the partial states of all pieces of a segment into one output row
-// (one query head `g` of kv head `w` of the group), one warp per row: lane j
-// of each round of 32 pieces computes piece j's slot and loads its m and l
-// (the rounds are usually one), the warp reduces the max with shuffles, then
-// every lane accumulates its D/32 dimensions over the pieces, eight pieces'
-// loads in flight at a time.
-template <int D, int G, int HG, int DT>
-__device__ void combine_row(const DecodeArgs &a, const CtaRange &rg, const Piece &pc, int w,
-                            int g, int lane) {
-  constexpr int PF = partial_floats(G, D), SLOT = HG * PF, DPL = D / 32;
+// Combine the partial states of all pieces of a segment into output rows
+// (row = query head g of kv head w of the group), one warp per NR rows, lane l
+// owning dimensions [l*D/32, (l+1)*D/32) of each. Pieces go in rounds of R
+// (the rounds are usually one); a round issues every load it needs -- each
+// row's and piece's m and l (the same address in all lanes) and the lane's
+// slice of the accumulator -- before using any of them, so a segment costs
+// one dependent round trip after the descriptor.
+template <int D, int G, int HG, int DT, int NR>
+__device__ void combine_rows(const DecodeArgs &a, const CtaRange &rg, const Piece &pc,
+                             const int (&rows)[NR], int lane) {
+  constexpr int PF = partial_floats(G, D), SLOT = HG * PF, DPL = D / 32, R = 2;
   const int cf = cta_of(pc.seg_start, rg), cl = cta_of(pc.seg_end - 1, rg);
   const int npc = cl - cf + 1;
-  float A[DPL];
+  float A[NR][DPL], M[NR], Ls[NR];
 #pragma unroll
-  for (int e = 0; e < DPL; ++e) A[e] = 0.f;
-  float M = -INFINITY;  // running max over the rounds
-  float Ls = 0.f;       // lane-partial sum of l * 2^(m - M)
-  for (int c0 = 0; c0 < npc; c0 += 32) {
-    const int cj = cf + c0 + lane;
-    const float *pj = cj <= cl ? partial_slot(a, cj, pc.seg_start, rg, SLOT) + w * PF : nullptr;
-    const float mj = pj ? __ldcg(pj + g) : -INFINITY;
-    const float lj = pj ? __ldcg(pj + G + g) : 0.f;
-    float Mr = mj;
+  for (int k = 0; k < NR; ++k) {
+    M[k] = -INFINITY;
+    Ls[k] = 0.f;
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) Mr = fmaxf(Mr, __shfl_xor_sync(0xffffffffu, Mr, o));
-    const float Mn = fmaxf(M, Mr);
-    const float rescale = (M == -INFINITY) ? 0.f : exp2f(M - Mn);  // earlier rounds
+    for (int e = 0; e < DPL; ++e) A[k][e] = 0.f;
+  }
+  for (int c0 = 0; c0 < npc; c0 += R) {
+    const int cnt = min(R, npc - c0);
+    float m[NR][R], l[NR][R], v[NR][R][DPL];
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) A[e] *= rescale;
-    Ls *= rescale;
-    M = Mn;
-    const float fj = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
-    Ls = __fmaf_rn(lj, fj, Ls);
-    const int cnt = min(32, npc - c0);
-    for (int j0 = 0; j0 < cnt; j0 += 8) {
-      float v[8][DPL];
-      float f[8];
+    for (int u = 0; u < R; ++u) {
+      const float *slot = partial_slot(a, cf + c0 + min(u, cnt - 1), pc.seg_start, rg, SLOT);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = min(j0 + u, cnt - 1);
-        const float *pu = reinterpret_cast<const float *>(
-            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(pj), j));
-        f[u] = (j0 + u < cnt) ? __shfl_sync(0xffffffffu, fj, j) : 0.f;
+      for (int k = 0; k < NR; ++k) {
+        const int w = rows[k] / G, g = rows[k] % G;
+        const float *p = slot + w * PF;
+        m[k][u] = __ldcg(p + g);
+        l[k][u] = __ldcg(p + G + g);
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) v[u][e] = __ldcg(pu + 2 * G + g * D + lane * DPL + e);
+        for (int e = 0; e < DPL; ++e) v[k][u][e] = __ldcg(p + 2 * G + g * D + lane * DPL + e);
       }
+    }
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
+    for (int k = 0; k < NR; ++k) {
+      float Mr = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) A[e] = __fmaf_rn(v[u][e], f[u], A[e]);
+      for (int u = 0; u < R; ++u)
+        if (u < cnt) Mr = fmaxf(Mr, m[k][u]);
+      const float Mn = fmaxf(M[k], Mr);
+      if (Mn == -INFINITY) continue;  // nothing but empty pieces so far
+      const float rescale = (M[k] == -INFINITY) ? 0.f : exp2f(M[k] - Mn);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) A[k][e] *= rescale;
+      Ls[k] *= rescale;
+      M[k] = Mn;
+#pragma unroll
+      for (int u = 0; u < R; ++u) {
+        const float f = (u < cnt && m[k][u] != -INFINITY) ? exp2f(m[k][u] - Mn) : 0.f;
+        Ls[k] = __fmaf_rn(l[k][u], f, Ls[k]);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) A[k][e] = __fmaf_rn(v[k][u][e], f, A[k][e]);
+      }
     }
   }
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-  const int h = pc.hg * HG + w;
-  uint16_t *orow = a.out + ((int64_t)pc.r * a.Hq + (int64_t)h * G + g) * D + lane * DPL;
+  for (int k = 0; k < NR; ++k) {
+    const int w = rows[k] / G, g = rows[k] % G;
+    const float inv = Ls[k] > 0.f ? 1.f / Ls[k] : 0.f;
+    const int h = pc.hg * HG + w;
+    uint16_t *orow = a.out + ((int64_t)pc.r * a.Hq + (int64_t)h * G + g) * D + lane * DPL;
 #pragma unroll
-  for (int e = 0; e < DPL; e += 2)
-    *reinterpret_cast<uint32_t *>(orow + e) = pack2<DT>(A[e] * inv, A[e + 1] * inv);
+    for (int e = 0; e < DPL; e += 2)
+      *reinterpret_cast<uint32_t *>(orow + e) = pack2<DT>(A[k][e] * inv, A[k][e + 1] * inv);
+  }
 }
 
-// The combine pass: grid (decode CTAs, row groups); block (x, y) combines
-// rows 4y .. 4y+3 (one per warp) of the segment described by decode CTA x.
-constexpr int COMBINE_ROWS = 4;
+// The combine pass: one CTA of COMBINE_WARPS warps per decode CTA; CTA x
+// combines the segment described by decode CTA x (if any), warp w taking rows
+// w, w + COMBINE_WARPS, ... of its HG*G rows, two at a time. Small
+// enough to wait, resident, beside the decode CTAs (programmatic launch).
+constexpr int COMBINE_WARPS = 8;
 template <int D, int G, int HG, int DT>
-__global__ void __launch_bounds__(COMBINE_ROWS * 32) decode_combine_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(COMBINE_WARPS * 32) decode_combine_kernel(DecodeArgs a) {
   griddep_wait();  // the split-K pass complete, its partials and descriptors visible
+  griddep_launch_dependents();
   const int *d = a.desc + blockIdx.x * DESC_INTS;
   if (!d[0]) return;
-  const int row = blockIdx.y * COMBINE_ROWS + (threadIdx.x >> 5);
-  if (row >= HG * G) return;
   Piece pc;
   pc.r = d[1];
   pc.hg = d[2];
@@ -464,25 +474,47 @@ __global__ void __launch_bounds__(COMBINE_ROWS * 32) decode_combine_kernel(Decod
   CtaRange rg;
   rg.n_eff = d[5];
   rg.Ptot = d[6];
-  combine_row<D, G, HG, DT>(a, rg, pc, row / G, row % G, threadIdx.x & 31);
+  constexpr int ROWS = HG * G, RPW = (ROWS + COMBINE_WARPS - 1) / COMBINE_WARPS;
+  constexpr int NR = RPW < 2 ? RPW : 2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int k0 = 0; k0 < RPW; k0 += NR) {
+    int rows[NR];
+    bool any = false;
+#pragma unroll
+    for (int k = 0; k < NR; ++k) {
+      const int row = warp + COMBINE_WARPS * (k0 + k);
+      rows[k] = row < ROWS ? row : warp;  // past the end: redo a valid row, same result
+      any |= row < ROWS;
+    }
+    if (any) combine_rows<D, G, HG, DT, NR>(a, rg, pc, rows, lane);
+  }
 }
 
-// Launch the combine pass for a split-K grid of `ctas` CTAs on stream s, as a
-// programmatic dependent of the kernel launched just before it: its CTAs may
-// be scheduled while that kernel runs and wait for it in griddep_wait.
-template <int D, int G, int HG, int DT>
-cudaError_t launch_combine(const DecodeArgs &a, int ctas, cudaStream_t s) {
+// Launch `kern` on stream s as a programmatic dependent of the kernel launched
+// just before it: its CTAs may be scheduled while that kernel still runs
+// (once that kernel's CTAs have all called griddep_launch_dependents), and
+// they wait for its completion in griddep_wait before reading anything.
+template <class... P, class... A>
+cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       A &&...args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ctas, (HG * G + COMBINE_ROWS - 1) / COMBINE_ROWS);
-  cfg.blockDim = dim3(COMBINE_ROWS * 32);
-  cfg.dynamicSmemBytes = 0;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, G, HG, DT>, a);
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<A &&>(args)...);
+}
+
+// the combine pass for a split-K grid of `ctas` CTAs
+template <int D, int G, int HG, int DT>
+cudaError_t launch_combine(const DecodeArgs &a, int ctas, cudaStream_t s) {
+  return launch_pdl(decode_combine_kernel<D, G, HG, DT>, dim3(ctas), dim3(COMBINE_WARPS * 32), 0,
+                    s, a);
 }
 
 }  // namespace kvinj

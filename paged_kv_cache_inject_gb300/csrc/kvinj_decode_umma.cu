@@ -489,8 +489,7 @@ static cudaError_t launch_umma_cfg(const DecodeArgs &a, const CUtensorMap &tmK,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<ctas, 256, smem, s>>>(tmK, tmV, a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(kern, dim3(ctas), dim3(256), smem, s, tmK, tmV, a);
   if (e != cudaSuccess) return e;
   return launch_combine<128, G, 8, DT>(a, ctas, s);
 }
