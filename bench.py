@@ -58,6 +58,40 @@ def _dist():
     return ws, rank, local
 
 
+# ---------------------------------------------------------------------------
+# replicas: nothing on the path exchanges data between GPUs; each rank runs
+# its own batch and only the timing is reduced
+# ---------------------------------------------------------------------------
+def workload_config(cfg) -> dict:
+    """The workload's identity in the JSON line (shared by both arms)."""
+    return {"workload": cfg.name, "layers": cfg.layers, "q_heads": cfg.q_heads,
+            "kv_heads": cfg.kv_heads, "head_dim": cfg.head_dim, "block_size": cfg.block_size,
+            "batch": cfg.batch, "context": list(cfg.ctx),
+            "injected_chunks_per_request": cfg.chunks_per_req, "chunk_len": cfg.chunk_len,
+            "pool_chunks": cfg.pool_chunks, "decode_steps": cfg.steps}
+
+
+def replica_seed(cfg_seed: int, rank: int) -> int:
+    """Seed of rank `rank`'s batch: an independent replica per rank."""
+    return cfg_seed + 1000 * rank
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The maximum of a per-rank scalar over all ranks (the job's time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, bytes_per_rank: int, ms: float) -> float:
+    """Bytes of all ranks (equal per-rank work) over the slowest rank's time."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
 
@@ -234,7 +268,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": args.config, "sample": "layer 0"},
+        "data": "synthetic",
+        "config": {**workload_config(wl.cfg), "sample": "layer 0 per step (oracle on host cores)"},
         "cpu_baseline": cpu,
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "inject_tokens_per_s": sample.inj_tokens / dt,
@@ -263,7 +298,7 @@ def run_gpu(args):
     cfg = W.CONFIGS[args.config]
     if args.layers:
         cfg = cfg.scaled(layers=args.layers)  # batch structure does not depend on L
-    wl = W.make_workload(cfg, seed=cfg.seed + 1000 * rank)  # independent replica per rank
+    wl = W.make_workload(cfg, seed=replica_seed(cfg.seed, rank))  # independent replica per rank
     remap = None
     if args.compact_pool:
         pool, remap = stage.compact_pool(wl, dev)
@@ -316,13 +351,9 @@ def run_gpu(args):
             run_step()
         t_end.record(stream)
         barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if ws > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
     ms_step = elapsed_ms / args.steps
-    value = ws * nbytes["total"] / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(ws, nbytes["total"], ms_step)
 
     # per-kernel timing: inject (all layers, one launch) and decode (one
     # launch pair -- split-K pass + combine -- per layer)
@@ -383,12 +414,8 @@ def run_gpu(args):
             eng.step_from_host(host, inp, out, host_out, g0)
         e1.record(stream)
         barrier()
-        e_ms = e0.elapsed_time(e1) / args.steps
-        if ws > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": ws * nbytes["total"] / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+        e2e = {"value": whole_job_gbs(ws, nbytes["total"], e_ms), "unit": "GB/s",
                "ms_per_step": e_ms, "h2d_bytes_per_step": host.nbytes,
                "d2h_bytes_per_step": host_out.numel() * host_out.element_size()}
     if eng.status.item() != 0:
@@ -398,11 +425,17 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu_baseline:
         threads = oracle_threads()
         sample = OracleSample(wl, threads)
-        t0 = time.perf_counter()
-        sample.run()
-        dt = time.perf_counter() - t0
-        cpu = {"value": sample.bytes / dt / 1e9, "unit": "GB/s", "cores": threads,
-               "kind": "oracle", "sample": sample.description, "seconds": dt}
+        # about ten seconds of oracle work: the layer-0 sample, repeated
+        runs, t0 = 0, time.perf_counter()
+        while True:
+            sample.run()
+            runs += 1
+            dt = time.perf_counter() - t0
+            if dt >= 10.0:
+                break
+        cpu = {"value": sample.bytes * runs / dt / 1e9, "unit": "GB/s", "cores": threads,
+               "kind": "oracle", "sample": f"{sample.description}; {runs} runs in {dt:.1f} s",
+               "seconds": dt}
 
     if rank != 0:
         return
@@ -411,12 +444,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": W.DTYPE_NAMES[cfg.dtype],
         "data": "synthetic",
-        "config": {"workload": cfg.name, "layers": cfg.layers, "q_heads": cfg.q_heads,
-                   "kv_heads": cfg.kv_heads, "head_dim": cfg.head_dim,
-                   "block_size": cfg.block_size, "batch": cfg.batch,
-                   "context": list(cfg.ctx), "injected_chunks_per_request": cfg.chunks_per_req,
-                   "chunk_len": cfg.chunk_len, "pool_chunks": cfg.pool_chunks,
-                   "decode_steps": cfg.steps, "parallelism": f"replicas x{ws}",
+        "config": {**workload_config(cfg), "parallelism": f"replicas x{ws}",
                    "l2": (f"inputs larger than L2: {nbytes['total'] / 1e9:.2f} GB touched per "
                           f"step; no flush"),
                    "decode_variant": args.variant,
