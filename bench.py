@@ -364,10 +364,17 @@ def run_gpu(args):
         eng.inject(inp.chunk_ids, inp.start_pos, slots[:n_inj_tok])
 
     def decode_only():
+        # the layer calls as the step makes them (append fused into decode by default;
+        # re-appending the same token writes the same bits)
         for s in range(cfg.steps):
             for layer in range(cfg.layers):
-                eng.decode(layer, inp.q[s, layer], inp.q_pos[s], inp.block_tables,
-                           inp.ctx_lens[s], out[s, layer])
+                if eng.fused_append:
+                    eng.append_decode(layer, inp.q[s, layer], inp.k_new[s, layer],
+                                      inp.v_new[s, layer], inp.q_pos[s], inp.block_tables,
+                                      inp.ctx_lens[s], out[s, layer])
+                else:
+                    eng.decode(layer, inp.q[s, layer], inp.q_pos[s], inp.block_tables,
+                               inp.ctx_lens[s], out[s, layer])
 
     def part_ms(fn, reps):
         g = None
@@ -390,13 +397,14 @@ def run_gpu(args):
 
     inj_avg = part_ms(inject_only, max(3, args.steps))
     dec_avg = part_ms(decode_only, max(3, args.steps)) / (cfg.layers * cfg.steps)
-    per_launch_decode = nbytes["decode"] / (cfg.layers * cfg.steps)
+    dec_bytes = nbytes["decode"] + (nbytes["append"] if eng.fused_append else 0)
+    per_launch_decode = dec_bytes / (cfg.layers * cfg.steps)
     dec_gbs = per_launch_decode / (dec_avg * 1e-3) / 1e9
     inj_gbs = nbytes["inject"] / (inj_avg * 1e-3) / 1e9
     inj_tok_s = wl.n_inj * cfg.chunk_len / (inj_avg * 1e-3)
     peak, peak_kind = _peaks()
-    # slot mapping + inject, then per step and layer: append, split-K decode, combine
-    launches_per_step = 2 + 3 * cfg.layers * cfg.steps
+    # slot mapping + inject, then per step and layer the append + decode launches
+    launches_per_step = 2 + eng.launches_per_layer() * cfg.layers * cfg.steps
 
     # end to end through host buffers (pinned), same metric
     e2e = None

@@ -154,9 +154,9 @@ int kvinj_append(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer
                  kvinj_stream_t stream);
 
 /* Workspace bytes kvinj_paged_decode needs for this shape on the current
- * device: one descriptor per CTA of the split-K grid (the segment it closes)
- * and two partial softmax states (m, l and the unnormalised output of every
- * query head of a head group) per CTA. */
+ * device: per CTA slot of the split-K grid, one descriptor (the segment it
+ * closes) and two partial softmax states (m, l and the unnormalised output of
+ * every query head of a head group). */
 size_t kvinj_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim);
 
@@ -181,7 +181,8 @@ int kvinj_decode_workspace_init(void *workspace, size_t ws_bytes, kvinj_stream_t
  * of the RoPE table leaves q unrotated (KVINJ_ST_BAD_POS). Requires
  * block_size 16, D 64 or 128, Hq % Hkv == 0, Hq/Hkv <= 16 and batch <= 4096
  * (KVINJ_EUNSUPPORTED otherwise). Launches two kernels on `stream`: the
- * split-K pass and the combine of the segments it cut. */
+ * split-K pass and the combine of the segments it cut (a programmatic
+ * dependent of the first). */
 int kvinj_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
                        int32_t num_q_heads, const void *q, const int32_t *q_pos,
                        const int32_t *block_tables, int32_t max_blocks,
@@ -204,6 +205,35 @@ int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int3
                           const int32_t *context_lens, int32_t batch, float scale, void *out,
                           void *workspace, size_t ws_bytes, int32_t *dev_status,
                           kvinj_stream_t stream, int32_t variant, int32_t ctas);
+
+/* Append, then decode ([KC] "The fix": each step appends the new token's K
+ * and V, then attends over the whole cache). For request r < batch the token
+ * at position q_pos[r] -- k_new/v_new[r]: device [batch][Hkv][D], pre-RoPE K --
+ * is written to k/v[layer] at slot block_tables[r][q_pos/16]*16 + q_pos%16
+ * (K rotated at q_pos, as kvinj_append does), and then every request is
+ * decoded exactly as kvinj_paged_decode does; context_lens[r] counts the new
+ * token (normally q_pos[r] + 1). Same result as kvinj_append with those slots
+ * followed by kvinj_paged_decode. With the tcgen05 kernel the append is part
+ * of the split-K pass: the CTA that reads the new token's block writes it
+ * first (no separate append launch). q_pos must be
+ * given; a position outside the RoPE table or a block-table entry outside the
+ * cache is skipped and flagged (KVINJ_ST_BAD_POS / KVINJ_ST_BAD_BLOCK).
+ * Other arguments and errors as kvinj_paged_decode / kvinj_paged_decode_ex. */
+int kvinj_append_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                              int32_t num_q_heads, const void *q, const void *k_new,
+                              const void *v_new, const int32_t *q_pos,
+                              const int32_t *block_tables, int32_t max_blocks,
+                              const int32_t *context_lens, int32_t batch, float scale,
+                              void *out, void *workspace, size_t ws_bytes, int32_t *dev_status,
+                              kvinj_stream_t stream);
+int kvinj_append_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope,
+                                 int32_t layer, int32_t num_q_heads, const void *q,
+                                 const void *k_new, const void *v_new, const int32_t *q_pos,
+                                 const int32_t *block_tables, int32_t max_blocks,
+                                 const int32_t *context_lens, int32_t batch, float scale,
+                                 void *out, void *workspace, size_t ws_bytes,
+                                 int32_t *dev_status, kvinj_stream_t stream, int32_t variant,
+                                 int32_t ctas);
 
 /* Paged decode without a caller-provided workspace (no counterpart in the
  * pages; an addition of this library). For callers that cannot allocate

@@ -209,6 +209,8 @@ int kvinj_append(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer
   a.v_new = static_cast<const uint16_t *>(v_new);
   a.positions = positions;
   a.slot_mapping = slot_mapping;
+  a.block_tables = nullptr;
+  a.max_blocks = 0;
   a.n = n;
   a.rope = rope ? static_cast<const float4 *>(rope->table) : nullptr;
   a.max_pos = rope ? rope->max_pos : 0;
@@ -233,12 +235,17 @@ int kvinj_decode_workspace_init(void *workspace, size_t ws_bytes, kvinj_stream_t
   return cuda_rc(cudaMemsetAsync(workspace, 0, ws_bytes, (cudaStream_t)stream));
 }
 
-int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
-                          int32_t num_q_heads, const void *q, const int32_t *q_pos,
-                          const int32_t *block_tables, int32_t max_blocks,
-                          const int32_t *context_lens, int32_t batch, float scale, void *out,
-                          void *workspace, size_t ws_bytes, int32_t *dev_status,
-                          kvinj_stream_t stream, int32_t variant, int32_t ctas) {
+namespace {
+
+// shared by the decode entry points: validate, pick the kernel, launch. With
+// k_new/v_new (fused append), the token of request r at q_pos[r] is written
+// first, at the slot its block table gives.
+int decode_call(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                int32_t num_q_heads, const void *q, const void *k_new, const void *v_new,
+                const int32_t *q_pos, const int32_t *block_tables, int32_t max_blocks,
+                const int32_t *context_lens, int32_t batch, float scale, void *out,
+                void *workspace, size_t ws_bytes, int32_t *dev_status, kvinj_stream_t stream,
+                int32_t variant, int32_t ctas) {
   int rc = check_cache(cache, true);
   if (rc) return rc;
   const int D = cache->head_dim, Hkv = cache->num_kv_heads;
@@ -249,6 +256,9 @@ int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int3
   if (batch == 0) return KVINJ_OK;
   if (!q || !block_tables || !context_lens || !out || !workspace) return KVINJ_EINVAL;
   if (rope && !q_pos) return KVINJ_EINVAL;
+  const bool append = k_new != nullptr || v_new != nullptr;
+  if (append && (!k_new || !v_new || !q_pos || !aligned16(k_new) || !aligned16(v_new)))
+    return KVINJ_EINVAL;
   if (!aligned16(q) || !aligned16(out)) return KVINJ_EINVAL;
   if (variant < 0 || variant > 3) return KVINJ_EINVAL;
   const bool g_pow2_8 = G == 1 || G == 2 || G == 4 || G == 8;
@@ -266,6 +276,28 @@ int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int3
   if (ctas < 0 || ctas > max_ctas) return KVINJ_EINVAL;
   if (ctas == 0) ctas = num_sms();
 
+  if (append && variant != 3) {
+    // the other kernels take no fused append: the append kernel runs first
+    AppendArgs p;
+    p.k = static_cast<uint16_t *>(cache->k);
+    p.v = static_cast<uint16_t *>(cache->v);
+    p.Hkv = Hkv;
+    p.num_blocks = cache->num_blocks;
+    p.B = cache->block_size;
+    p.layer = layer;
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
+    p.positions = q_pos;
+    p.slot_mapping = nullptr;
+    p.block_tables = block_tables;
+    p.max_blocks = max_blocks;
+    p.n = batch;
+    p.rope = rope ? static_cast<const float4 *>(rope->table) : nullptr;
+    p.max_pos = rope ? rope->max_pos : 0;
+    p.status = dev_status;
+    if ((rc = cuda_rc(launch_append(p, D, cache->dtype, (cudaStream_t)stream)))) return rc;
+  }
+
   const int HG = decode_head_group(Hkv);
   CUtensorMap tmK, tmV;
   if ((rc = make_cache_map(&tmK, cache->k, cache, HG))) return rc;
@@ -281,6 +313,10 @@ int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int3
   a.out = static_cast<uint16_t *>(out);
   a.desc = static_cast<int *>(workspace);
   a.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + decode_desc_bytes());
+  a.k_new = append && variant == 3 ? static_cast<const uint16_t *>(k_new) : nullptr;
+  a.v_new = append && variant == 3 ? static_cast<const uint16_t *>(v_new) : nullptr;
+  a.k_cache = static_cast<uint16_t *>(cache->k);
+  a.v_cache = static_cast<uint16_t *>(cache->v);
   a.status = dev_status;
   a.batch = batch;
   a.Hq = num_q_heads;
@@ -292,6 +328,45 @@ int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int3
   a.scale_log2 = (float)(sc * 1.4426950408889634);
   return cuda_rc(launch_decode(a, tmK, tmV, D, G, HG, cache->dtype, variant, ctas,
                                (cudaStream_t)stream));
+}
+
+}  // namespace
+
+int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                          int32_t num_q_heads, const void *q, const int32_t *q_pos,
+                          const int32_t *block_tables, int32_t max_blocks,
+                          const int32_t *context_lens, int32_t batch, float scale, void *out,
+                          void *workspace, size_t ws_bytes, int32_t *dev_status,
+                          kvinj_stream_t stream, int32_t variant, int32_t ctas) {
+  return decode_call(cache, rope, layer, num_q_heads, q, nullptr, nullptr, q_pos, block_tables,
+                     max_blocks, context_lens, batch, scale, out, workspace, ws_bytes,
+                     dev_status, stream, variant, ctas);
+}
+
+int kvinj_append_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope,
+                                 int32_t layer, int32_t num_q_heads, const void *q,
+                                 const void *k_new, const void *v_new, const int32_t *q_pos,
+                                 const int32_t *block_tables, int32_t max_blocks,
+                                 const int32_t *context_lens, int32_t batch, float scale,
+                                 void *out, void *workspace, size_t ws_bytes,
+                                 int32_t *dev_status, kvinj_stream_t stream, int32_t variant,
+                                 int32_t ctas) {
+  if (!k_new || !v_new) return KVINJ_EINVAL;
+  return decode_call(cache, rope, layer, num_q_heads, q, k_new, v_new, q_pos, block_tables,
+                     max_blocks, context_lens, batch, scale, out, workspace, ws_bytes,
+                     dev_status, stream, variant, ctas);
+}
+
+int kvinj_append_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                              int32_t num_q_heads, const void *q, const void *k_new,
+                              const void *v_new, const int32_t *q_pos,
+                              const int32_t *block_tables, int32_t max_blocks,
+                              const int32_t *context_lens, int32_t batch, float scale,
+                              void *out, void *workspace, size_t ws_bytes, int32_t *dev_status,
+                              kvinj_stream_t stream) {
+  return kvinj_append_paged_decode_ex(cache, rope, layer, num_q_heads, q, k_new, v_new, q_pos,
+                                      block_tables, max_blocks, context_lens, batch, scale, out,
+                                      workspace, ws_bytes, dev_status, stream, 0, 0);
 }
 
 int kvinj_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,

@@ -40,6 +40,8 @@ struct DecodeLayout {
   static constexpr int QB = QB_;                        // q staging buffers (0 = none)
   static constexpr int EMPTY_ARRIVALS = HG;             // consumer warps free a stage
   static constexpr bool QPOS_SM = false;  // q positions copied to shared memory after pre[]
+  static constexpr bool APPEND_WAIT = false;  // the producer waits for a fused append
+  static constexpr int off_qfull = 0, QBUF = 1;
   static constexpr int NBOX = D / 64;                   // 64-element (128-byte) column boxes
   static constexpr int BOXB = HG * BLK * 128;           // bytes of one box: HG*16 rows
   static constexpr int UNIT_BYTES = NBOX * BOXB;        // K (or V) of one unit
@@ -166,7 +168,7 @@ __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) 
     int v = 0;
     if (r < a.batch) {
       // both loads in flight together, before any shared-memory store
-      const int qp = (Lay::QPOS_SM && a.rope) ? __ldg(a.q_pos + r) : -1;
+      const int qp = (Lay::QPOS_SM && a.q_pos) ? __ldg(a.q_pos + r) : -1;
       const int c = __ldg(a.context_lens + r);
       if constexpr (Lay::QPOS_SM) reinterpret_cast<int *>(sm + Lay::off_pre)[a.batch + 1 + r] = qp;
       v = ((c > 0 && c <= a.max_blocks * BLK) ? (c + BLK - 1) / BLK : 0) * ngrp;
@@ -250,12 +252,13 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
   const int n = rg.b1 - rg.b0;
   // lookup of unit g0 + lane: block-table entry (and, when q is staged, the
   // request's q position); the loads are consumed one batch later
-  auto start_lookup = [&](int gi, int &blk, int &hg, int &rq, int &first, int &qp) {
+  auto start_lookup = [&](int gi, int &blk, int &hg, int &rq, int &first, int &qp, int &ap) {
     blk = -1;
     hg = 0;
     rq = 0;
     first = 0;
     qp = -1;
+    ap = 0;
     if (gi < n) {
       const int P = rg.b0 + gi;
       const int r = find_request(pre, a.batch, P);
@@ -267,11 +270,16 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
       first = (gi == 0 || pg == 0) ? 1 : 0;  // first unit of a piece
       blk = a.block_tables[(int64_t)r * a.max_blocks + pg];
       if (Lay::QB && first && a.rope) qp = a.q_pos[r];
+      if constexpr (Lay::APPEND_WAIT) {
+        // this unit holds the token appended by this call (written by the query warps)
+        const int qa = pre[a.batch + 1 + r];
+        ap = (a.k_new && qa >= 0 && (!a.rope || qa < a.max_pos) && qa / BLK == pg) ? 1 : 0;
+      }
     }
   };
-  int blk, hg, rq, first, qp;
-  start_lookup(lane, blk, hg, rq, first, qp);
-  int issued = 0, pieces = 0;
+  int blk, hg, rq, first, qp, ap;
+  start_lookup(lane, blk, hg, rq, first, qp, ap);
+  int issued = 0, pieces = 0, cur_piece = -1;
   bool aborted = false;
   for (int g0 = 0; g0 < n && !aborted; g0 += 32) {
     const int ok = (blk >= 0 && blk < a.num_blocks) ? 1 : 0;
@@ -281,8 +289,8 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
     const int qpos_ok = (qp >= 0 && qp < a.max_pos) ? qp : -1;
     if (Lay::QB && first && a.rope && qpos_ok < 0 && g0 + lane < n) report(a.status, KVINJ_ST_BAD_POS);
     const int qrow0 = rq * a.Hq + hg * HG * Lay::G;  // first q row of the head group
-    int nblk, nhg, nrq, nfirst, nqp;
-    start_lookup(g0 + 32 + lane, nblk, nhg, nrq, nfirst, nqp);
+    int nblk, nhg, nrq, nfirst, nqp, nap;
+    start_lookup(g0 + 32 + lane, nblk, nhg, nrq, nfirst, nqp, nap);
     const int cnt = min(32, n - g0);
     for (int i = 0; i < cnt; ++i) {
       const int r0 = __shfl_sync(0xffffffffu, row0, i);
@@ -290,9 +298,20 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
       const int fi = __shfl_sync(0xffffffffu, first, i);
       const int qri = __shfl_sync(0xffffffffu, qrow0, i);
       const int qpi = __shfl_sync(0xffffffffu, qpos_ok, i);
+      const int api = __shfl_sync(0xffffffffu, ap, i);
       const int gi = g0 + i, st = gi % S;
       int go = 1;
+      if (fi) ++cur_piece;
       if (lane == 0) {
+        if constexpr (Lay::APPEND_WAIT) {
+          // the piece's query warps write the appended token before its block is read
+          uint64_t *qf = reinterpret_cast<uint64_t *>(sm + Lay::off_qfull) + cur_piece % Lay::QBUF;
+          if (api && !flags[0] &&
+              !mbar_wait_bounded(qf, (uint32_t)(cur_piece / Lay::QBUF) & 1u)) {
+            report(a.status, KVINJ_ST_TIMEOUT);
+            flags[0] = 1;
+          }
+        }
         if (Lay::QB && fi && !flags[0]) {
           // q rows (and RoPE row) of the piece starting here
           constexpr int QBD = Lay::QB ? Lay::QB : 1;
@@ -346,6 +365,7 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
     rq = nrq;
     first = nfirst;
     qp = nqp;
+    ap = nap;
   }
   if (aborted && lane == 0) {
     // let the copies already in flight land before the CTA can exit

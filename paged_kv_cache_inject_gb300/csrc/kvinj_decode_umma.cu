@@ -64,6 +64,7 @@ struct UmmaLayout {
   static constexpr int QBUF = QBUF_;         // Q tiles, written by the query warps
   static constexpr int EMPTY_ARRIVALS = 1;   // one MMA commit frees a stage
   static constexpr bool QPOS_SM = true;      // the query warps read q positions there
+  static constexpr bool APPEND_WAIT = true;  // the producer waits for a fused append
   static constexpr int N = HG * 2 * G;       // MMA N
   static constexpr int NBOX = D / 64;
   static constexpr int BOXB = HG * BLK * 128;          // 16 KiB
@@ -79,6 +80,7 @@ struct UmmaLayout {
   // sfull[2] sfree[2] pfull pvdone qfull[QBUF] qempty[QBUF] ofree done
   static constexpr int NXBAR = 8 + 2 * QBUF;
   static constexpr int off_xbar = off_bar + 2 * S * 8;
+  static constexpr int off_qfull = off_xbar + 6 * 8;  // qfull[QBUF] (see below)
   static constexpr int off_valid = off_xbar + NXBAR * 8;
   static constexpr int off_qinfo = off_valid + S * 4;  // unused
   static constexpr int off_flags = off_qinfo + 16;
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(256, 1)
       const Piece pc = find_piece(a, pre, ngrp, P, rg.b1);
       const int qbuf = piece % QBUF;
       // the loads (query rows, RoPE row) go out before the wait for the tile
-      int qp = qpos_sm[pc.r];
+      int qp = a.rope ? qpos_sm[pc.r] : -1;
       if (a.rope && (qp < 0 || qp >= a.max_pos)) {
         if (qw == 0 && lane == 0) report(a.status, KVINJ_ST_BAD_POS);
         qp = -1;
@@ -259,6 +261,25 @@ __global__ void __launch_bounds__(256, 1)
         const uint16_t *row = qg + (int64_t)(2 * k + qw) * D;
         xw[k] = __ldg(reinterpret_cast<const unsigned int *>(row + 2 * lane));
         yw[k] = __ldg(reinterpret_cast<const unsigned int *>(row + 64 + 2 * lane));
+      }
+      // fused append: the token at q_pos, if its block is one of this piece's
+      // units, is written here (K rotated at q_pos with the same table row)
+      const int qa = qpos_sm[pc.r];
+      const int pg_a = qa >= 0 ? qa / BLK : -1;
+      const bool app = a.k_new && qa >= 0 && (!a.rope || qa < a.max_pos) && pg_a >= pc.pg0 &&
+                       pg_a < pc.pg0 + (pc.end - P);
+      uint32_t akx[HG / 2], aky[HG / 2], avx[HG / 2], avy[HG / 2];
+      int64_t abl = -1;
+      if (app) {
+        abl = a.block_tables[(int64_t)pc.r * a.max_blocks + pg_a];
+#pragma unroll
+        for (int k = 0; k < HG / 2; ++k) {
+          const int64_t src = ((int64_t)pc.r * a.Hkv + pc.hg * HG + qw * (HG / 2) + k) * D;
+          akx[k] = __ldg(reinterpret_cast<const unsigned int *>(a.k_new + src + 2 * lane));
+          aky[k] = __ldg(reinterpret_cast<const unsigned int *>(a.k_new + src + 64 + 2 * lane));
+          avx[k] = __ldg(reinterpret_cast<const unsigned int *>(a.v_new + src + 2 * lane));
+          avy[k] = __ldg(reinterpret_cast<const unsigned int *>(a.v_new + src + 64 + 2 * lane));
+        }
       }
       bool ok = true;
       if (piece >= QBUF) ok = wait(qempty + qbuf, (uint32_t)(piece / QBUF - 1) & 1u);
@@ -287,6 +308,32 @@ __global__ void __launch_bounds__(256, 1)
           sts32(qt + tile_off<N>(nh, 64 + 2 * lane), yh);
           sts32(qt + tile_off<N>(nl, 2 * lane), xl);
           sts32(qt + tile_off<N>(nl, 64 + 2 * lane), yl);
+        }
+        if (app) {
+          if (abl < 0 || abl >= a.num_blocks) {
+            if (lane == 0) report(a.status, KVINJ_ST_BAD_BLOCK);
+          } else {
+#pragma unroll
+            for (int k = 0; k < HG / 2; ++k) {
+              const int h = pc.hg * HG + qw * (HG / 2) + k;
+              const int64_t dst =
+                  ((((int64_t)a.layer * a.num_blocks + abl) * a.Hkv + h) * BLK + qa % BLK) * D;
+              uint32_t kx = akx[k], ky = aky[k];
+              if (a.rope) {
+                const float2 x = unpack2<DT>(kx), y = unpack2<DT>(ky);
+                const float2 r0 = rope_pair(x.x, y.x, t0);
+                const float2 r1 = rope_pair(x.y, y.y, t1);
+                kx = pack2<DT>(r0.x, r1.x);
+                ky = pack2<DT>(r0.y, r1.y);
+              }
+              st_global(reinterpret_cast<uint32_t *>(a.k_cache + dst + 2 * lane), kx);
+              st_global(reinterpret_cast<uint32_t *>(a.k_cache + dst + 64 + 2 * lane), ky);
+              st_global(reinterpret_cast<uint32_t *>(a.v_cache + dst + 2 * lane), avx[k]);
+              st_global(reinterpret_cast<uint32_t *>(a.v_cache + dst + 64 + 2 * lane), avy[k]);
+            }
+            // these generic stores precede the producer's tensor copy of the block
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+          }
         }
         fence_async_smem();
       }

@@ -189,11 +189,19 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   const int64_t row = (int64_t)a.Hkv * D;
   const int64_t nslots = a.num_blocks * a.B;
   for (int64_t i = warp; i < a.n; i += nwarps) {
-    const int64_t slot = a.slot_mapping[i];
     const int pos = a.positions[i];
     int bad = 0;
-    if (slot < 0 || slot >= nslots) bad |= KVINJ_ST_BAD_SLOT;
     if (pos < 0 || (a.rope && pos >= a.max_pos)) bad |= KVINJ_ST_BAD_POS;
+    int64_t slot;
+    if (a.slot_mapping) {
+      slot = a.slot_mapping[i];
+    } else {  // token i of request i, slot from the request's block table
+      const int pg = pos >= 0 ? pos / a.B : 0;
+      const int64_t blk = pg < a.max_blocks ? a.block_tables[i * a.max_blocks + pg] : -1;
+      slot = blk >= 0 && blk < a.num_blocks ? blk * a.B + (pos % a.B) : -1;
+      if (slot < 0) bad |= KVINJ_ST_BAD_BLOCK;
+    }
+    if (!(bad & KVINJ_ST_BAD_BLOCK) && (slot < 0 || slot >= nslots)) bad |= KVINJ_ST_BAD_SLOT;
     if (bad) {
       if (lane == 0) report(a.status, bad);
       continue;

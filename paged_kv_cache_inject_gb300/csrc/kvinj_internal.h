@@ -33,7 +33,9 @@ struct AppendArgs {
   int B, layer;
   const uint16_t *k_new, *v_new;
   const int32_t *positions;
-  const int64_t *slot_mapping;
+  const int64_t *slot_mapping;  // nullptr: slot of token i from its block table (below)
+  const int32_t *block_tables;  // [n][max_blocks] when slot_mapping is nullptr
+  int max_blocks;
   int64_t n;
   const float4 *rope;  // nullptr: keys already rotated
   int max_pos;
@@ -50,6 +52,8 @@ struct DecodeArgs {
   uint16_t *out;               // [batch][Hq][D]
   float *partials;             // [2*max_ctas][HG][G][D+2]
   int *desc;                   // [max_ctas][8] cut-segment descriptors
+  const uint16_t *k_new, *v_new;  // [batch][Hkv][D]: token appended at q_pos (nullptr: none)
+  uint16_t *k_cache, *v_cache;    // cache bases, written by the append
   int32_t *status;
   int batch, Hq, Hkv, max_blocks, layer;
   int64_t num_blocks;

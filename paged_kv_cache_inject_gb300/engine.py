@@ -6,7 +6,8 @@ all layers, the RoPE table and the decode workspace -- and runs one step of
 the hot path through the library's kernels:
 
     slot mapping -> inject (all layers) -> per decode step, per layer:
-    append the new token's K/V, paged decode attention
+    append the new token's K/V, paged decode attention (one fused call:
+    kvinj_append_paged_decode)
 
 Every operation here is a call into libkvinj.so; this module only sequences
 the calls and owns the buffers. ``step_from_host`` is the end-to-end form a
@@ -62,6 +63,7 @@ class Engine:
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.decode_variant = 0
         self.decode_ctas = 0
+        self.fused_append = True  # append + decode in one call
 
     # -- single operations ---------------------------------------------------
     def slot_mapping(self, block_tables, seq, pos, out=None):
@@ -82,6 +84,25 @@ class Engine:
         K.kvinj_paged_decode_ex(self.cache, self.rope if rotate else None, layer, q, q_pos,
                                 block_tables, ctx_lens, out, self.workspace, 0.0, self.status,
                                 None, self.decode_variant, self.decode_ctas)
+
+    def append_decode(self, layer, q, k_new, v_new, q_pos, block_tables, ctx_lens, out,
+                      rotate=True):
+        K.kvinj_append_paged_decode(self.cache, self.rope if rotate else None, layer, q, k_new,
+                                    v_new, q_pos, block_tables, ctx_lens, out, self.workspace,
+                                    0.0, self.status, None, self.decode_variant,
+                                    self.decode_ctas)
+
+    def uses_tcgen05(self) -> bool:
+        """Whether decode runs the tcgen05 kernel (one launch per layer)."""
+        G = self.Hq // self.Hkv
+        ok = self.D == 128 and self.Hkv % 8 == 0 and G in (1, 2, 4, 8)
+        return self.decode_variant == 3 or (self.decode_variant == 0 and ok)
+
+    def launches_per_layer(self) -> int:
+        """Kernel launches of one layer's append + decode."""
+        if self.uses_tcgen05() and self.fused_append:
+            return 2  # split-K pass with the append, combine pass
+        return 3  # append, split-K pass, combine pass
 
     # -- one step of the hot path --------------------------------------------
     def alloc_outputs(self, steps: int) -> torch.Tensor:
@@ -105,6 +126,16 @@ class Engine:
         step_slots = slots[n_inj_tok:n_tok].view(steps, self.batch)
         for s in range(steps):
             for layer in range(self.L):
+                if self.fused_append:
+                    # the step token's slot is the one its block table gives
+                    if timer:
+                        timer("decode", 0)
+                    self.append_decode(layer, inp.q[s, layer], inp.k_new[s, layer],
+                                       inp.v_new[s, layer], inp.q_pos[s], inp.block_tables,
+                                       inp.ctx_lens[s], out[s, layer])
+                    if timer:
+                        timer("decode", 1)
+                    continue
                 self.append(layer, inp.k_new[s, layer], inp.v_new[s, layer], inp.q_pos[s],
                             step_slots[s])
                 if timer:

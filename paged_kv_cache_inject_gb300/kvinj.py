@@ -27,7 +27,8 @@ ST_BAD_CTX, ST_BAD_SEQ, ST_TIMEOUT = 0x10, 0x20, 0x40
 EXPORTS = [
     "kvinj_rope_table_bytes", "kvinj_rope_table_host", "kvinj_slot_mapping", "kvinj_inject",
     "kvinj_append", "kvinj_decode_workspace_size", "kvinj_decode_workspace_init",
-    "kvinj_paged_decode", "kvinj_paged_decode_ex", "kvinj_paged_decode_static", "kvinj_kv_bytes",
+    "kvinj_paged_decode", "kvinj_paged_decode_ex", "kvinj_append_paged_decode",
+    "kvinj_append_paged_decode_ex", "kvinj_paged_decode_static", "kvinj_kv_bytes",
     "kvinj_strerror",
 ]
 
@@ -84,6 +85,11 @@ def load(path: str = LIB_PATH):
                                                   ctypes.c_float, P, P, sz, P, P]),
             "kvinj_paged_decode_ex": (ctypes.c_int, [P, P, i32, i32, P, P, P, i32, P, i32,
                                                      ctypes.c_float, P, P, sz, P, P, i32, i32]),
+            "kvinj_append_paged_decode": (ctypes.c_int, [P, P, i32, i32, P, P, P, P, P, i32, P,
+                                                         i32, ctypes.c_float, P, P, sz, P, P]),
+            "kvinj_append_paged_decode_ex": (ctypes.c_int, [P, P, i32, i32, P, P, P, P, P, i32,
+                                                            P, i32, ctypes.c_float, P, P, sz, P,
+                                                            P, i32, i32]),
             "kvinj_paged_decode_static": (ctypes.c_int, [P, P, i32, i32, P, P, P, i32, P, i32,
                                                          ctypes.c_float, P, P, P]),
             "kvinj_kv_bytes": (i64, [i32, i32, i32, i64, i32]),
@@ -286,4 +292,21 @@ def kvinj_paged_decode_ex(cache: Cache, rope: Rope | None, layer: int, q, q_pos,
                                         float(scale), _ptr(out), _ptr(workspace),
                                         workspace.numel() * workspace.element_size(),
                                         _ptr(status), _stream(stream), variant, ctas))
+    return out
+
+
+def kvinj_append_paged_decode(cache: Cache, rope: Rope | None, layer: int, q, k_new, v_new,
+                              q_pos, block_tables, context_lens, out, workspace,
+                              scale: float = 0.0, status=None, stream=None, variant: int = 0,
+                              ctas: int = 0):
+    """Append the token at q_pos of every request (k_new, v_new [batch][Hkv][D]), then
+    decode; variant/ctas as in kvinj_paged_decode_ex (0: automatic)."""
+    batch, Hq, _ = q.shape
+    _check("kvinj_append_paged_decode_ex",
+           load().kvinj_append_paged_decode_ex(
+               cache.ref, rope.ref if rope is not None else None, layer, Hq, _ptr(q),
+               _ptr(k_new), _ptr(v_new), _ptr(q_pos), _ptr(block_tables), block_tables.shape[1],
+               _ptr(context_lens), batch, float(scale), _ptr(out), _ptr(workspace),
+               workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream),
+               variant, ctas))
     return out

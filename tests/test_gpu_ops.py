@@ -450,3 +450,94 @@ def test_decode_umma_refuses_shapes_it_does_not_cover():
             _run_decode(kc, vc, q, bt, np.array([20], np.int32), np.array([19], np.int32), dt, 0,
                         1e4, 40, variant=3)
         assert e.value.code == K.KVINJ_EUNSUPPORTED
+
+
+# ---------------------------------------------------------------------------
+# append + decode in one call
+# ---------------------------------------------------------------------------
+def _fused_case(D, G, dt, ctx, Hkv, seed, rotate=True):
+    kc, vc, q, bt = _decode_case(D, G, dt, ctx, Hkv=Hkv, L=2, seed=seed)
+    batch = len(ctx)
+    kn = gen_bits(seed + 5, (batch, Hkv, D), dt)
+    vn = gen_bits(seed + 6, (batch, Hkv, D), dt)
+    ctx = np.asarray(ctx, np.int32)
+    pos = ctx - 1  # the new token is the newest one of the context
+    slots = bt[np.arange(batch), pos // 16].astype(np.int64) * 16 + pos % 16
+    theta = 5e5
+    ek, ev = kc.copy(), vc.copy()
+    oracle.append(ek, ev, 1, kn, vn, pos, slots, theta, dt, rotate=rotate)
+    want, st = oracle.paged_decode(ek, ev, 1, q, pos, bt, ctx, theta, dt, rotate_q=rotate)
+    assert st == 0
+    return kc, vc, q, bt, kn, vn, ctx, pos, slots, theta, ek, ev, want
+
+
+def _run_fused(kc, vc, q, bt, kn, vn, ctx, pos, dt, theta, variant, ctas, rotate=True,
+               status=None):
+    tdt = torch_dtype(dt)
+    D = kc.shape[-1]
+    cache = K.Cache(from_bits(kc, tdt), from_bits(vc, tdt))
+    rope = K.make_rope(theta, D, int(ctx.max()) + 4) if rotate else None
+    batch, Hq, _ = q.shape
+    ws = K.make_decode_workspace(batch, Hq, kc.shape[2], D)
+    out = torch.full((batch, Hq, D), float("nan"), dtype=tdt, device="cuda")
+    K.kvinj_append_paged_decode(cache, rope, 1, from_bits(q, tdt), from_bits(kn, tdt),
+                                from_bits(vn, tdt), i32(pos), i32(bt), i32(ctx), out, ws, 0.0,
+                                status, None, variant, ctas)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64), bits(cache.k), bits(cache.v)
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("ctas", [0, 1, 5, 37])
+@pytest.mark.parametrize("G,Hkv", [(4, 8), (1, 16), (8, 8)])
+def test_append_paged_decode_matches_oracle(variant, ctas, G, Hkv):
+    D, dt = 128, W.BF16
+    ctx = [1, 16, 17, 250, 611, 33]
+    kc, vc, q, bt, kn, vn, ctx, pos, slots, theta, ek, ev, want = _fused_case(
+        D, G, dt, ctx, Hkv, seed=90 + G + Hkv)
+    status = status_tensor()
+    got, gk, gv = _run_fused(kc, vc, q, bt, kn, vn, ctx, pos, dt, theta, variant, ctas,
+                             status=status)
+    assert status.item() == 0
+    assert np.array_equal(gv, ev)
+    assert ulp_distance(gk, ek).max() <= 1
+    assert_decode_close(got, want, f"fused variant{variant} ctas{ctas} G{G} Hkv{Hkv}")
+
+
+def test_append_paged_decode_equals_separate_calls_bitwise():
+    D, G, dt, Hkv = 128, 4, W.BF16, 8
+    ctx = [700, 33, 1500, 16, 2048, 5]
+    kc, vc, q, bt, kn, vn, ctx, pos, slots, theta, ek, ev, want = _fused_case(
+        D, G, dt, ctx, Hkv, seed=97)
+    got, gk, gv = _run_fused(kc, vc, q, bt, kn, vn, ctx, pos, dt, theta, 3, 0)
+    tdt = torch_dtype(dt)
+    cache = K.Cache(from_bits(kc, tdt), from_bits(vc, tdt))
+    rope = K.make_rope(theta, D, int(ctx.max()) + 4)
+    K.kvinj_append(cache, rope, 1, from_bits(kn, tdt), from_bits(vn, tdt), i32(pos),
+                   torch.from_numpy(slots).cuda())
+    ws = K.make_decode_workspace(len(ctx), Hkv * G, Hkv, D)
+    out = torch.empty((len(ctx), Hkv * G, D), dtype=tdt, device="cuda")
+    K.kvinj_paged_decode_ex(cache, rope, 1, from_bits(q, tdt), i32(pos), i32(bt), i32(ctx), out,
+                            ws, 0.0, None, None, 3, 0)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(cache.k), gk) and np.array_equal(bits(cache.v), gv)
+    assert np.array_equal(out.float().cpu().numpy().astype(np.float64), got)
+
+
+@pytest.mark.parametrize("variant", [2, 3])
+def test_append_paged_decode_unrotated_and_bad_block(variant):
+    D, G, dt, Hkv = 128, 4, W.BF16, 8
+    ctx = [40, 300, 17]
+    kc, vc, q, bt, kn, vn, ctx, pos, slots, theta, ek, ev, want = _fused_case(
+        D, G, dt, ctx, Hkv, seed=98, rotate=False)
+    got, gk, gv = _run_fused(kc, vc, q, bt, kn, vn, ctx, pos, dt, theta, variant, 0, rotate=False)
+    assert np.array_equal(gk, ek) and np.array_equal(gv, ev)
+    assert_decode_close(got, want, f"fused unrotated variant{variant}")
+    # the new token's page outside the cache: flagged, other requests intact
+    bt2 = bt.copy()
+    bt2[0, pos[0] // 16] = kc.shape[1] + 3
+    status = status_tensor()
+    got, gk, gv = _run_fused(kc, vc, q, bt2, kn, vn, ctx, pos, dt, theta, variant, 0,
+                             rotate=False, status=status)
+    assert status.item() & K.ST_BAD_BLOCK
+    assert_decode_close(got[1:], want[1:], f"fused bad block variant{variant}")
