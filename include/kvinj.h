@@ -80,6 +80,7 @@ typedef struct CUstream_st *kvinj_stream_t; /* a cudaStream_t */
 #define KVINJ_ST_BAD_CTX 0x10   /* context length <= 0 or > max_blocks*block_size */
 #define KVINJ_ST_BAD_SEQ 0x20   /* sequence id outside [0, batch)              */
 #define KVINJ_ST_TIMEOUT 0x40   /* a pipeline wait gave up (kernel returned early) */
+#define KVINJ_ST_INTERNAL 0x80  /* a launch precondition failed on the device (no output) */
 
 /* paged KV cache of one model (all layers) */
 typedef struct {
@@ -154,15 +155,15 @@ int kvinj_append(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer
                  kvinj_stream_t stream);
 
 /* Workspace bytes kvinj_paged_decode needs for this shape on the current
- * device: per CTA slot of the split-K grid, one descriptor (the segment it
- * closes) and two partial softmax states (m, l and the unnormalised output of
- * every query head of a head group). */
+ * device: per CTA slot of the split-K grid, two partial softmax states (m, l
+ * and the unnormalised output of every query head of a head group), after a
+ * small reserved header. */
 size_t kvinj_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim);
 
-/* Zero a decode workspace. Optional: every decode call writes each
- * descriptor and partial state before reading it, so the workspace may hold
- * anything; zeroing only makes its contents deterministic for inspection. */
+/* Zero a decode workspace. Optional: every decode call writes each partial
+ * state before reading it, so the workspace may hold anything; zeroing only
+ * makes its contents deterministic for inspection. */
 int kvinj_decode_workspace_init(void *workspace, size_t ws_bytes, kvinj_stream_t stream);
 
 /* Paged decode attention ("LLM Inference: KV Caching", attention and Paged

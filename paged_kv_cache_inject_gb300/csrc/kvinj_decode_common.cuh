@@ -16,12 +16,11 @@
 // segment of ceil(C_r/16) units. Units are flattened request-major and cut
 // into gridDim.x equal contiguous ranges, one per CTA. A segment inside one
 // CTA range is finished there; a segment cut by range boundaries leaves one
-// partial softmax state per piece in the workspace. The CTA whose range holds
-// the last unit of a cut segment records a descriptor of it, and a second,
-// small kernel launched after this one on the same stream combines the
-// pieces (stream order makes every partial visible to it). The streaming
-// kernel thus needs no fence, atomic or counter, and nothing waits on
-// another CTA.
+// partial softmax state per piece in the workspace, and a second, small
+// kernel launched after this one on the same stream combines the pieces
+// (stream order makes every partial visible to it; which pieces make up a
+// segment follows from the context lengths alone). The streaming kernel thus
+// needs no fence, atomic or counter, and nothing waits on another CTA.
 #pragma once
 
 #include <math.h>
@@ -123,27 +122,47 @@ __device__ __forceinline__ Piece find_piece(const DecodeArgs &a, const int *pre,
   return pc;
 }
 
-// Descriptor of the cut segment (if any) whose last unit lies in this CTA's
-// range: only the segment holding the range's first unit can have started
-// before the range. Written by thread 0 of every CTA of the grid (CTAs
-// without units write "none").
-constexpr int DESC_INTS = 8;  // valid, r, hg, seg_start, seg_end, n_eff, Ptot, -
-__device__ __forceinline__ void write_descriptor(const DecodeArgs &a, const int *pre, int ngrp,
-                                                 const CtaRange *rg) {
-  int *d = a.desc + blockIdx.x * DESC_INTS;
-  if (!rg) {
-    d[0] = 0;
-    return;
+// Units per request -> pre[0..batch] (exclusive prefix sums, in shared
+// memory), by all NT threads of the CTA. `units(r, c)` gives request r's units
+// from its context length c (and may act on it); `scratch` holds NT/32 ints.
+template <int NT, class F>
+__device__ void unit_prefix(const DecodeArgs &a, int *pre, int *scratch, F units) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NWARP = NT / 32;
+  int carry = 0;
+  for (int base = 0; base < a.batch; base += NT) {
+    const int r = base + tid;
+    const int v = r < a.batch ? units(r, __ldg(a.context_lens + r)) : 0;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < NWARP ? scratch[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < NWARP) scratch[lane] = w;
+    }
+    __syncthreads();
+    const int incl = x + (warp > 0 ? scratch[warp - 1] : 0);
+    if (r < a.batch) pre[r + 1] = carry + incl;
+    carry += scratch[NWARP - 1];
+    __syncthreads();
   }
-  const Piece pc = find_piece(a, pre, ngrp, rg->b0, rg->b1);
-  const bool ends_cut = pc.seg_start < rg->b0 && pc.seg_end <= rg->b1;
-  d[0] = ends_cut ? 1 : 0;
-  d[1] = pc.r;
-  d[2] = pc.hg;
-  d[3] = pc.seg_start;
-  d[4] = pc.seg_end;
-  d[5] = rg->n_eff;
-  d[6] = rg->Ptot;
+  if (tid == 0) pre[0] = 0;
+  __syncthreads();
+}
+
+// 16-token blocks of a valid context (0 for an invalid one)
+__device__ __forceinline__ int context_pages(const DecodeArgs &a, int c) {
+  return (c > 0 && c <= a.max_blocks * BLK) ? (c + BLK - 1) / BLK : 0;
 }
 
 // Units per request -> prefix sums pre[0..batch], this CTA's range, barrier
@@ -158,60 +177,23 @@ __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) 
   griddep_launch_dependents();
   int *pre = reinterpret_cast<int *>(sm + Lay::off_pre);
   int *flags = reinterpret_cast<int *>(sm + Lay::off_flags);
-  int *ws = flags + 8;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int NWARP = NT / 32;
+  const int tid = threadIdx.x;
   const int ngrp = a.Hkv / Lay::HG;
-  int carry = 0;
-  for (int base = 0; base < a.batch; base += NT) {
-    const int r = base + tid;
-    int v = 0;
-    if (r < a.batch) {
-      // both loads in flight together, before any shared-memory store
-      const int qp = (Lay::QPOS_SM && a.q_pos) ? __ldg(a.q_pos + r) : -1;
-      const int c = __ldg(a.context_lens + r);
-      if constexpr (Lay::QPOS_SM) reinterpret_cast<int *>(sm + Lay::off_pre)[a.batch + 1 + r] = qp;
-      v = ((c > 0 && c <= a.max_blocks * BLK) ? (c + BLK - 1) / BLK : 0) * ngrp;
-      if (v == 0 && blockIdx.x == 0) {
-        uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t)r * a.Hq * Lay::D);
-        for (int i = 0; i < a.Hq * Lay::D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
-        report(a.status, KVINJ_ST_BAD_CTX);
-      }
+  unit_prefix<NT>(a, pre, flags + 8, [&](int r, int c) {
+    if constexpr (Lay::QPOS_SM) pre[a.batch + 1 + r] = a.q_pos ? __ldg(a.q_pos + r) : -1;
+    const int v = context_pages(a, c) * ngrp;
+    if (v == 0 && blockIdx.x == 0) {
+      uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t)r * a.Hq * Lay::D);
+      for (int i = 0; i < a.Hq * Lay::D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+      report(a.status, KVINJ_ST_BAD_CTX);
     }
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) ws[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      int w = lane < NWARP ? ws[lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += y;
-      }
-      if (lane < NWARP) ws[lane] = w;
-    }
-    __syncthreads();
-    const int incl = x + (warp > 0 ? ws[warp - 1] : 0);
-    if (r < a.batch) pre[r + 1] = carry + incl;
-    carry += ws[NWARP - 1];
-    __syncthreads();
-  }
-  if (tid == 0) pre[0] = 0;
-  __syncthreads();
+    return v;
+  });
   rg.Ptot = pre[a.batch];
   rg.n_eff = min((int)gridDim.x, rg.Ptot);
-  if ((int)blockIdx.x >= rg.n_eff) {
-    if (tid == 0) write_descriptor(a, pre, ngrp, nullptr);
-    return false;
-  }
+  if ((int)blockIdx.x >= rg.n_eff) return false;
   rg.b0 = range_begin(blockIdx.x, rg);
   rg.b1 = range_begin(blockIdx.x + 1, rg);
-  if (tid == 0) write_descriptor(a, pre, ngrp, &rg);
   if (tid == 0) {
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + Lay::off_bar);
     for (int s = 0; s < Lay::S; ++s) {
@@ -477,28 +459,38 @@ __device__ void combine_rows(const DecodeArgs &a, const CtaRange &rg, const Piec
 
 // The combine pass: grid (decode CTAs, ceil(HG*G / COMBINE_WARPS)), one warp
 // per output row: CTA (x, y) combines rows COMBINE_WARPS*y .. +COMBINE_WARPS-1
-// of the segment described by decode CTA x (if any), four pieces' loads in
-// flight per round. Small enough to wait, resident, beside the decode CTAs
-// (programmatic launch). (Measured against one CTA per segment with two rows
-// per warp: 43 vs 50 us per layer for the split-K pass + combine at batch 32.)
+// of the cut segment (if any) whose last unit lies in decode CTA x's range,
+// four pieces' loads in flight per round. Which segment that is depends only
+// on the context lengths, which the split-K pass read after its own
+// dependency wait (before it let this grid start): it is worked out before
+// this grid waits for that pass. Small enough to wait, resident, beside the
+// decode CTAs (programmatic launch). (Measured against one CTA per segment
+// with two rows per warp: 43 vs 50 us per layer for split-K pass + combine at
+// batch 32.)
 constexpr int COMBINE_WARPS = 8;
 template <int D, int G, int HG, int DT>
 __global__ void __launch_bounds__(COMBINE_WARPS * 32) decode_combine_kernel(DecodeArgs a) {
-  griddep_wait();  // the split-K pass complete, its partials and descriptors visible
-  griddep_launch_dependents();
-  const int *d = a.desc + blockIdx.x * DESC_INTS;
-  if (!d[0]) return;
-  Piece pc;
-  pc.r = d[1];
-  pc.hg = d[2];
-  pc.seg_start = d[3];
-  pc.seg_end = d[4];
+  extern __shared__ int comb_sm[];  // scratch[COMBINE_WARPS], pre[batch + 1]
+  int *pre = comb_sm + COMBINE_WARPS;
+  const int ngrp = a.Hkv / HG;
+  unit_prefix<COMBINE_WARPS * 32>(a, pre, comb_sm,
+                                  [&](int, int c) { return context_pages(a, c) * ngrp; });
   CtaRange rg;
-  rg.n_eff = d[5];
-  rg.Ptot = d[6];
+  rg.Ptot = pre[a.batch];
+  rg.n_eff = min((int)gridDim.x, rg.Ptot);
+  bool cut = false;
+  Piece pc;
+  if ((int)blockIdx.x < rg.n_eff) {
+    rg.b0 = range_begin(blockIdx.x, rg);
+    rg.b1 = range_begin(blockIdx.x + 1, rg);
+    pc = find_piece(a, pre, ngrp, rg.b0, rg.b1);
+    cut = pc.seg_start < rg.b0 && pc.seg_end <= rg.b1;
+  }
+  griddep_wait();  // the split-K pass complete, its partial states visible
+  griddep_launch_dependents();
   constexpr int ROWS = HG * G;
   const int row = blockIdx.y * COMBINE_WARPS + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (row >= ROWS) return;
+  if (!cut || row >= ROWS) return;
   const int rows[1] = {row};
   combine_rows<D, G, HG, DT, 1>(a, rg, pc, rows, lane);
 }
@@ -528,7 +520,7 @@ template <int D, int G, int HG, int DT>
 cudaError_t launch_combine(const DecodeArgs &a, int ctas, cudaStream_t s) {
   return launch_pdl(decode_combine_kernel<D, G, HG, DT>,
                     dim3(ctas, (HG * G + COMBINE_WARPS - 1) / COMBINE_WARPS),
-                    dim3(COMBINE_WARPS * 32), 0,
+                    dim3(COMBINE_WARPS * 32), (size_t)(COMBINE_WARPS + a.batch + 1) * sizeof(int),
                     s, a);
 }
 

@@ -91,7 +91,9 @@ struct UmmaLayout {
   // S[2] at columns 0 and N, O at 2N
   static constexpr uint32_t TMEM_COLS =
       3 * N <= 32 ? 32 : 3 * N <= 64 ? 64 : 3 * N <= 128 ? 128 : 3 * N <= 256 ? 256 : 512;
-  static size_t bytes(int batch) { return (size_t)off_pre + (size_t)(2 * batch + 1) * 4 + 1024; }
+  // the dynamic shared array is declared 1024-byte aligned: no slack for alignment (the
+  // bytes saved let a combine CTA stay resident beside this one)
+  static size_t bytes(int batch) { return (size_t)off_pre + (size_t)(2 * batch + 1) * 4; }
   static_assert(3 * N <= 512, "tensor memory: S[2] and O");
   static_assert(off_q % 1024 == 0 && off_p % 1024 == 0, "swizzle atoms are 1024-byte aligned");
 };
@@ -121,12 +123,13 @@ __global__ void __launch_bounds__(256, 1)
   constexpr int D = 128, HG = 8, N = Lay::N, PF = partial_floats(G, D), SLOT = HG * PF;
   static_assert(G == 1 || G == 2 || G == 4 || G == 8, "tcgen05 decode: G");
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *sm = align_smem(smem_raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *sm = smem_raw;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  CtaRange rg;
-  if (!decode_prologue<Lay, 256>(a, sm, rg)) return;
+  if (smem_u32(sm) & 1023u) {  // the swizzled tiles need 1024-byte alignment
+    if (tid == 0) report(a.status, KVINJ_ST_INTERNAL);
+    return;
+  }
 
   uint64_t *full = reinterpret_cast<uint64_t *>(sm + Lay::off_bar);
   uint64_t *empty = full + S;
@@ -135,6 +138,7 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t *qfull = sfull + 6, *qempty = qfull + QBUF, *ofree = qempty + QBUF, *done = ofree + 1;
   volatile int *flags = reinterpret_cast<volatile int *>(sm + Lay::off_flags);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + Lay::off_tmem);
+  // set-up that reads no input runs before the dependency wait (in the prologue)
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(sfull + b, 1);
@@ -154,9 +158,15 @@ __global__ void __launch_bounds__(256, 1)
     tmem_alloc(tslot, Lay::TMEM_COLS);
     tmem_relinquish();
   }
+  CtaRange rg;
+  const bool has_units = decode_prologue<Lay, 256>(a, sm, rg);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (!has_units) {
+    if (warp == 1) tmem_dealloc(*tslot, Lay::TMEM_COLS);
+    return;
+  }
   const uint32_t tbase = *tslot;
   const int *pre = reinterpret_cast<const int *>(sm + Lay::off_pre);
   const int ngrp = a.Hkv / HG;

@@ -51,7 +51,7 @@ struct DecodeArgs {
   int max_pos;
   uint16_t *out;               // [batch][Hq][D]
   float *partials;             // [2*max_ctas][HG][G][D+2]
-  int *desc;                   // [max_ctas][8] cut-segment descriptors
+  int *desc;                   // [max_ctas][8] reserved
   const uint16_t *k_new, *v_new;  // [batch][Hkv][D]: token appended at q_pos (nullptr: none)
   uint16_t *k_cache, *v_cache;    // cache bases, written by the append
   int32_t *status;

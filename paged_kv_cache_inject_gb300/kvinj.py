@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libkvinj.so")
 KVINJ_BF16, KVINJ_FP16 = 0, 1
 KVINJ_OK, KVINJ_EINVAL, KVINJ_EUNSUPPORTED, KVINJ_EWORKSPACE, KVINJ_ECUDA = 0, 1, 2, 3, 4
 ST_BAD_CHUNK, ST_BAD_SLOT, ST_BAD_BLOCK, ST_BAD_POS = 0x01, 0x02, 0x04, 0x08
-ST_BAD_CTX, ST_BAD_SEQ, ST_TIMEOUT = 0x10, 0x20, 0x40
+ST_BAD_CTX, ST_BAD_SEQ, ST_TIMEOUT, ST_INTERNAL = 0x10, 0x20, 0x40, 0x80
 
 EXPORTS = [
     "kvinj_rope_table_bytes", "kvinj_rope_table_host", "kvinj_slot_mapping", "kvinj_inject",
