@@ -306,6 +306,7 @@ def run_gpu(args):
     else:
         eng = stage.make_engine(wl, dev)
     eng.decode_variant = args.variant
+    eng.overlap_inject = args.overlap_inject
     stage.fill_context(eng, wl, dev)
     inp = stage.step_inputs(wl, dev)
     if remap is not None:
@@ -403,8 +404,10 @@ def run_gpu(args):
     inj_gbs = nbytes["inject"] / (inj_avg * 1e-3) / 1e9
     inj_tok_s = wl.n_inj * cfg.chunk_len / (inj_avg * 1e-3)
     peak, peak_kind = _peaks()
-    # slot mapping + inject, then per step and layer the append + decode launches
-    launches_per_step = 2 + eng.launches_per_layer() * cfg.layers * cfg.steps
+    # slot mapping, inject (one launch, or one per layer when overlapped), then per step and
+    # layer the append + decode launches
+    inject_launches = cfg.layers if eng.overlap_inject else 1
+    launches_per_step = 1 + inject_launches + eng.launches_per_layer() * cfg.layers * cfg.steps
 
     # end to end through host buffers (pinned), same metric
     e2e = None
@@ -456,6 +459,8 @@ def run_gpu(args):
                    "l2": (f"inputs larger than L2: {nbytes['total'] / 1e9:.2f} GB touched per "
                           f"step; no flush"),
                    "decode_variant": args.variant,
+                   "inject_schedule": ("per layer, low-priority stream beside the decode"
+                                       if eng.overlap_inject else "all layers, then decode"),
                    "launch": "cuda graph per step" if use_graph else "eager",
                    "pool": ("drawn chunks only" if args.compact_pool else
                             f"full, {cfg.pool_bytes / 1e9:.1f} GB resident")},
@@ -491,6 +496,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--variant", type=int, default=0, help="decode kernel: 0 auto, 1 FMA, 2 mma.sync, 3 tcgen05")
+    ap.add_argument("--overlap-inject", dest="overlap_inject", action="store_true",
+                    help="inject layer by layer on a low-priority stream beside the decode")
+    ap.add_argument("--serial", dest="overlap_inject", action="store_false",
+                    help="inject all layers, then decode (one stream)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly from Python")
     ap.add_argument("--layers", type=int, default=0,

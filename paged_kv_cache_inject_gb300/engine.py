@@ -64,6 +64,8 @@ class Engine:
         self.decode_variant = 0
         self.decode_ctas = 0
         self.fused_append = True  # append + decode in one call
+        self.overlap_inject = False  # inject on a low-priority stream beside the decode
+        self._hi = self._lo = None
 
     # -- single operations ---------------------------------------------------
     def slot_mapping(self, block_tables, seq, pos, out=None):
@@ -109,41 +111,76 @@ class Engine:
         return torch.empty((steps, self.L, self.batch, self.Hq, self.D), dtype=self.dtype,
                            device=self.device)
 
+    def _layer(self, s, layer, inp: StepInputs, out, step_slots, timer=None):
+        """Append + decode of one layer of decode step s."""
+        if self.fused_append:
+            # the step token's slot is the one its block table gives
+            if timer:
+                timer("decode", 0)
+            self.append_decode(layer, inp.q[s, layer], inp.k_new[s, layer], inp.v_new[s, layer],
+                               inp.q_pos[s], inp.block_tables, inp.ctx_lens[s], out[s, layer])
+            if timer:
+                timer("decode", 1)
+            return
+        self.append(layer, inp.k_new[s, layer], inp.v_new[s, layer], inp.q_pos[s], step_slots[s])
+        if timer:
+            timer("decode", 0)
+        self.decode(layer, inp.q[s, layer], inp.q_pos[s], inp.block_tables, inp.ctx_lens[s],
+                    out[s, layer])
+        if timer:
+            timer("decode", 1)
+
+    def _streams(self):
+        if self._hi is None:
+            # out-of-range priorities map to the device's highest / lowest
+            self._hi = torch.cuda.Stream(device=self.device, priority=-100)
+            self._lo = torch.cuda.Stream(device=self.device, priority=100)
+        return self._hi, self._lo
+
     def step(self, inp: StepInputs, out: torch.Tensor, timer=None):
         """slot mapping + inject + (append, decode) per step and layer.
+
+        With `overlap_inject` (and no timer), the inject runs layer by layer on a
+        low-priority stream while the decode layers run on a high-priority one;
+        decode of layer l waits for the inject of layer l only. The two are
+        independent HBM traffic: the inject fills the DRAM time the decode
+        launches leave idle (their start, tail and combine pass). The result is
+        the same as the serial order.
 
         `timer`, when given, is called as timer(kind, stream_event_pair_index)
         around the inject and decode launches (used for per-kernel timing)."""
         n_tok = inp.map_pos.numel()
         slots = self.slot_mapping(inp.block_tables, inp.map_seq, inp.map_pos)
         n_inj_tok = inp.chunk_ids.numel() * self.chunk_len
+        steps = inp.q.shape[0]
+        step_slots = slots[n_inj_tok:n_tok].view(steps, self.batch)
+        if self.overlap_inject and timer is None:
+            cur = torch.cuda.current_stream(self.device)
+            hi, lo = self._streams()
+            lo.wait_stream(cur)
+            hi.wait_stream(cur)
+            ready = [torch.cuda.Event() for _ in range(self.L)]
+            with torch.cuda.stream(lo):
+                for layer in range(self.L):
+                    self.inject(inp.chunk_ids, inp.start_pos, slots[:n_inj_tok], layer, layer + 1)
+                    ready[layer].record(lo)
+            with torch.cuda.stream(hi):
+                for s in range(steps):
+                    for layer in range(self.L):
+                        if s == 0:
+                            hi.wait_event(ready[layer])
+                        self._layer(s, layer, inp, out, step_slots)
+            cur.wait_stream(hi)
+            cur.wait_stream(lo)
+            return out
         if timer:
             timer("inject", 0)
         self.inject(inp.chunk_ids, inp.start_pos, slots[:n_inj_tok])
         if timer:
             timer("inject", 1)
-        steps = inp.q.shape[0]
-        step_slots = slots[n_inj_tok:n_tok].view(steps, self.batch)
         for s in range(steps):
             for layer in range(self.L):
-                if self.fused_append:
-                    # the step token's slot is the one its block table gives
-                    if timer:
-                        timer("decode", 0)
-                    self.append_decode(layer, inp.q[s, layer], inp.k_new[s, layer],
-                                       inp.v_new[s, layer], inp.q_pos[s], inp.block_tables,
-                                       inp.ctx_lens[s], out[s, layer])
-                    if timer:
-                        timer("decode", 1)
-                    continue
-                self.append(layer, inp.k_new[s, layer], inp.v_new[s, layer], inp.q_pos[s],
-                            step_slots[s])
-                if timer:
-                    timer("decode", 0)
-                self.decode(layer, inp.q[s, layer], inp.q_pos[s], inp.block_tables,
-                            inp.ctx_lens[s], out[s, layer])
-                if timer:
-                    timer("decode", 1)
+                self._layer(s, layer, inp, out, step_slots, timer)
         return out
 
     def capture(self, inp: StepInputs, out: torch.Tensor, timer=None) -> torch.cuda.CUDAGraph:

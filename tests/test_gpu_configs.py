@@ -117,3 +117,29 @@ def test_config_full_size(name):
         assert_decode_close(got, want, f"{name} step {s} layer {layer} req {r} head {qh}")
     del eng, pool, inp, out
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_b32", "llama3_70b_b8_8k"])
+def test_overlapped_inject_schedule_matches_serial_bitwise(name):
+    # inject layer by layer on a low-priority stream beside the decode: the same cache and
+    # outputs, bit for bit, as inject-then-decode on one stream (graph-captured, as timed)
+    from workload import stage
+    cfg = W.CONFIGS[name].scaled(layers=4, steps=min(W.CONFIGS[name].steps, 2))
+    wl = W.make_workload(cfg)
+    pool, remap = stage.compact_pool(wl)
+    results = []
+    for overlap in (False, True):
+        eng = stage.make_engine(wl, pool=pool)
+        eng.overlap_inject = overlap
+        stage.fill_context(eng, wl)
+        inp = stage.step_inputs(wl)
+        inp.chunk_ids.copy_(torch.from_numpy(remap).cuda())
+        out = eng.alloc_outputs(cfg.steps)
+        g = eng.capture(inp, out)
+        g.replay()
+        torch.cuda.synchronize()
+        assert eng.status.item() == 0
+        results.append((bits(out), bits(eng.k_cache), bits(eng.v_cache)))
+        del eng, g
+    for a, b in zip(*results):
+        assert np.array_equal(a, b)
