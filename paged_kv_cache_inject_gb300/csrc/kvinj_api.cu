@@ -327,6 +327,7 @@ int decode_call(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
   a.max_blocks = max_blocks;
   a.layer = layer;
   a.num_blocks = cache->num_blocks;
+  a.ctas = ctas;
   const double sc = scale > 0.f ? (double)scale : 1.0 / sqrt((double)D);
   a.scale_log2 = (float)(sc * 1.4426950408889634);
   return cuda_rc(launch_decode(a, tmK, tmV, D, G, HG, cache->dtype, variant, ctas,

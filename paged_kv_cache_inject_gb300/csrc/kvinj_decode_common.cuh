@@ -457,16 +457,19 @@ __device__ void combine_rows(const DecodeArgs &a, const CtaRange &rg, const Piec
   }
 }
 
-// The combine pass: grid (decode CTAs, ceil(HG*G / COMBINE_WARPS)), one warp
-// per output row: CTA (x, y) combines rows COMBINE_WARPS*y .. +COMBINE_WARPS-1
-// of the cut segment (if any) whose last unit lies in decode CTA x's range,
-// four pieces' loads in flight per round. Which segment that is depends only
-// on the context lengths, which the split-K pass read after its own
-// dependency wait (before it let this grid start): it is worked out before
-// this grid waits for that pass. Small enough to wait, resident, beside the
-// decode CTAs (programmatic launch). (Measured against one CTA per segment
-// with two rows per warp: 43 vs 50 us per layer for split-K pass + combine at
-// batch 32.)
+// The combine pass: grid (segments, ceil(HG*G / COMBINE_WARPS)), one warp per
+// output row: CTA (s, y) takes segment s = (request, head group) and, if the
+// split-K ranges cut it, combines its rows COMBINE_WARPS*y .. +COMBINE_WARPS-1,
+// four pieces' loads in flight per round. Whether and where a segment was cut
+// follows from the context lengths alone, which the split-K pass read after its
+// own dependency wait (before it let this grid start): that is worked out, and
+// the segment's partial-state lines are prefetched, before this grid waits for
+// the split-K pass. A grid of segments (a few per SM at serving batch sizes)
+// leaves its CTAs resident beside the decode CTAs, so only the loads of the
+// partial states follow the wait. (Measured at batch 32, split-K pass +
+// combine per layer: one CTA per segment with two rows per warp 50.5 us; one
+// warp per row over a grid of decode CTAs 42.9 us; this grid of segments: see
+// the design notes.)
 constexpr int COMBINE_WARPS = 8;
 template <int D, int G, int HG, int DT>
 __global__ void __launch_bounds__(COMBINE_WARPS * 32) decode_combine_kernel(DecodeArgs a) {
@@ -477,20 +480,33 @@ __global__ void __launch_bounds__(COMBINE_WARPS * 32) decode_combine_kernel(Deco
                                   [&](int, int c) { return context_pages(a, c) * ngrp; });
   CtaRange rg;
   rg.Ptot = pre[a.batch];
-  rg.n_eff = min((int)gridDim.x, rg.Ptot);
-  bool cut = false;
+  rg.n_eff = min(a.ctas, rg.Ptot);
   Piece pc;
-  if ((int)blockIdx.x < rg.n_eff) {
-    rg.b0 = range_begin(blockIdx.x, rg);
-    rg.b1 = range_begin(blockIdx.x + 1, rg);
-    pc = find_piece(a, pre, ngrp, rg.b0, rg.b1);
-    cut = pc.seg_start < rg.b0 && pc.seg_end <= rg.b1;
+  pc.r = blockIdx.x / ngrp;
+  pc.hg = blockIdx.x % ngrp;
+  const int pages = (pre[pc.r + 1] - pre[pc.r]) / ngrp;
+  pc.seg_start = pre[pc.r] + pc.hg * pages;
+  pc.seg_end = pc.seg_start + pages;
+  constexpr int ROWS = HG * G, PF = partial_floats(G, D), SLOT = HG * PF;
+  const int row = blockIdx.y * COMBINE_WARPS + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int cf = pages > 0 ? cta_of(pc.seg_start, rg) : 0;
+  const int cl = pages > 0 ? cta_of(pc.seg_end - 1, rg) : 0;
+  if (cf == cl) return;  // finished inside one split-K range (or empty)
+  if (row < ROWS) {
+    // warm L2 and the address translations for this row's partial states while the
+    // split-K pass still runs (a hint: the lines it writes later are current in L2)
+    const int w = row / G, g = row % G;
+    const int j = lane & 7;  // per piece: m/l, then the D-float slice (up to 5 lines)
+    if (j <= 5) {
+      for (int c = cf + (lane >> 3); c <= cl; c += 4) {
+        const float *p = partial_slot(a, c, pc.seg_start, rg, SLOT) + w * PF;
+        prefetch_l2(j == 0 ? p + g : p + 2 * G + g * D + min((j - 1) * 32, D - 1));
+      }
+    }
   }
   griddep_wait();  // the split-K pass complete, its partial states visible
   griddep_launch_dependents();
-  constexpr int ROWS = HG * G;
-  const int row = blockIdx.y * COMBINE_WARPS + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (!cut || row >= ROWS) return;
+  if (row >= ROWS) return;
   const int rows[1] = {row};
   combine_rows<D, G, HG, DT, 1>(a, rg, pc, rows, lane);
 }
@@ -518,10 +534,12 @@ cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, c
 // the combine pass for a split-K grid of `ctas` CTAs
 template <int D, int G, int HG, int DT>
 cudaError_t launch_combine(const DecodeArgs &a, int ctas, cudaStream_t s) {
+  DecodeArgs c = a;
+  c.ctas = ctas;
   return launch_pdl(decode_combine_kernel<D, G, HG, DT>,
-                    dim3(ctas, (HG * G + COMBINE_WARPS - 1) / COMBINE_WARPS),
+                    dim3(a.batch * (a.Hkv / HG), (HG * G + COMBINE_WARPS - 1) / COMBINE_WARPS),
                     dim3(COMBINE_WARPS * 32), (size_t)(COMBINE_WARPS + a.batch + 1) * sizeof(int),
-                    s, a);
+                    s, c);
 }
 
 }  // namespace kvinj

@@ -215,6 +215,11 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
       : "memory");
 }
 
+// hint: bring the line holding p into L2 (and its address translation)
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

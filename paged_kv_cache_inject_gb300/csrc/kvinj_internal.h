@@ -56,6 +56,7 @@ struct DecodeArgs {
   uint16_t *k_cache, *v_cache;    // cache bases, written by the append
   int32_t *status;
   int batch, Hq, Hkv, max_blocks, layer;
+  int ctas;                    // split-K grid size (set for the combine pass)
   int64_t num_blocks;
   float scale_log2;            // softmax scale times log2(e)
 };
