@@ -192,7 +192,7 @@ int kvinj_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t
                        kvinj_stream_t stream);
 
 /* Same as kvinj_paged_decode with an explicit kernel choice (G = Hq/Hkv):
- * variant 0 = automatic (3 where it applies and G <= 4, else 2 for G >= 4, else 1),
+ * variant 0 = automatic (3 where it applies, else 2 for G >= 4, else 1),
  * 1 = CUDA-core FMA kernel (G in {1, 2, 4, 8}),
  * 2 = warp-level mma.sync kernel (G in {1, 2, 4, 8, 16}),
  * 3 = tcgen05 kernel, accumulators in tensor memory (D = 128, Hkv a multiple

@@ -263,10 +263,10 @@ int decode_call(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
   if (variant < 0 || variant > 3) return KVINJ_EINVAL;
   const bool g_pow2_8 = G == 1 || G == 2 || G == 4 || G == 8;
   const bool umma_ok = D == 128 && decode_head_group(Hkv) == 8 && g_pow2_8;
-  // automatic: tcgen05 up to G = 4; at G = 8 its Q and P tiles leave room for two stages
-  // only, and the mma.sync kernel (three stages) streams faster (61 vs 78 us per layer at
-  // 8 requests x 8192 tokens, 64 q / 8 kv heads)
-  if (variant == 0) variant = (umma_ok && G <= 4) ? 3 : (G >= 4 ? 2 : 1);
+  // automatic: tcgen05 wherever it applies (at G = 8 with units of two blocks of 4 kv
+  // heads: 61.6 vs 69.6 us per layer for the mma.sync kernel at 8 requests x 8192
+  // tokens, 64 q / 8 kv heads), else mma.sync from G = 4 up, else the FMA kernel
+  if (variant == 0) variant = umma_ok ? 3 : (G >= 4 ? 2 : 1);
   if (variant == 1 && !g_pow2_8) return KVINJ_EUNSUPPORTED;
   if (variant == 2 && !(g_pow2_8 || G == 16)) return KVINJ_EUNSUPPORTED;
   if (variant == 3 && !umma_ok) return KVINJ_EUNSUPPORTED;
@@ -303,8 +303,11 @@ int decode_call(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
 
   const int HG = decode_head_group(Hkv);
   CUtensorMap tmK, tmV;
-  if ((rc = make_cache_map(&tmK, cache->k, cache, HG))) return rc;
-  if ((rc = make_cache_map(&tmV, cache->v, cache, HG))) return rc;
+  // boxes of HG heads of one block; the tcgen05 kernel at G = 8 places one head of one
+  // block per box (its units are two blocks of 4 kv heads)
+  const int box_heads = (variant == 3 && G == 8) ? 1 : HG;
+  if ((rc = make_cache_map(&tmK, cache->k, cache, box_heads))) return rc;
+  if ((rc = make_cache_map(&tmV, cache->v, cache, box_heads))) return rc;
 
   DecodeArgs a;
   a.q = static_cast<const uint16_t *>(q);

@@ -40,6 +40,7 @@ struct DecodeLayout {
   static constexpr int EMPTY_ARRIVALS = HG;             // consumer warps free a stage
   static constexpr bool QPOS_SM = false;  // q positions copied to shared memory after pre[]
   static constexpr bool APPEND_WAIT = false;  // the producer waits for a fused append
+  static constexpr int BPU = 1;               // 16-token blocks per unit
   static constexpr int off_qfull = 0, QBUF = 1;
   static constexpr int NBOX = D / 64;                   // 64-element (128-byte) column boxes
   static constexpr int BOXB = HG * BLK * 128;           // bytes of one box: HG*16 rows
@@ -164,6 +165,11 @@ __device__ void unit_prefix(const DecodeArgs &a, int *pre, int *scratch, F units
 __device__ __forceinline__ int context_pages(const DecodeArgs &a, int c) {
   return (c > 0 && c <= a.max_blocks * BLK) ? (c + BLK - 1) / BLK : 0;
 }
+// work units of one head group of a request whose context is c tokens long
+template <int BPU>
+__device__ __forceinline__ int context_units(const DecodeArgs &a, int c) {
+  return (context_pages(a, c) + BPU - 1) / BPU;
+}
 
 // Units per request -> prefix sums pre[0..batch], this CTA's range, barrier
 // set-up. CTA 0 also zeroes the output of requests whose context length is
@@ -181,7 +187,7 @@ __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) 
   const int ngrp = a.Hkv / Lay::HG;
   unit_prefix<NT>(a, pre, flags + 8, [&](int r, int c) {
     if constexpr (Lay::QPOS_SM) pre[a.batch + 1 + r] = a.q_pos ? __ldg(a.q_pos + r) : -1;
-    const int v = context_pages(a, c) * ngrp;
+    const int v = context_units<Lay::BPU>(a, c) * ngrp;
     if (v == 0 && blockIdx.x == 0) {
       uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t)r * a.Hq * Lay::D);
       for (int i = 0; i < a.Hq * Lay::D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
@@ -234,8 +240,11 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
   const int n = rg.b1 - rg.b0;
   // lookup of unit g0 + lane: block-table entry (and, when q is staged, the
   // request's q position); the loads are consumed one batch later
-  auto start_lookup = [&](int gi, int &blk, int &hg, int &rq, int &first, int &qp, int &ap) {
+  // with two blocks per unit, blk2 is the second one (-2: the context ends before it)
+  auto start_lookup = [&](int gi, int &blk, int &blk2, int &hg, int &rq, int &first, int &qp,
+                          int &ap) {
     blk = -1;
+    blk2 = -2;
     hg = 0;
     rq = 0;
     first = 0;
@@ -250,32 +259,44 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
       const int pg = off - hg * pages;
       rq = r;
       first = (gi == 0 || pg == 0) ? 1 : 0;  // first unit of a piece
-      blk = a.block_tables[(int64_t)r * a.max_blocks + pg];
+      blk = a.block_tables[(int64_t)r * a.max_blocks + pg * Lay::BPU];
+      if constexpr (Lay::BPU == 2) {
+        if (pg * 2 + 1 < context_pages(a, __ldg(a.context_lens + r)))
+          blk2 = a.block_tables[(int64_t)r * a.max_blocks + pg * 2 + 1];
+      }
       if (Lay::QB && first && a.rope) qp = a.q_pos[r];
       if constexpr (Lay::APPEND_WAIT) {
         // this unit holds the token appended by this call (written by the query warps)
         const int qa = pre[a.batch + 1 + r];
-        ap = (a.k_new && qa >= 0 && (!a.rope || qa < a.max_pos) && qa / BLK == pg) ? 1 : 0;
+        ap = (a.k_new && qa >= 0 && (!a.rope || qa < a.max_pos) && qa / BLK / Lay::BPU == pg)
+                 ? 1 : 0;
       }
     }
   };
-  int blk, hg, rq, first, qp, ap;
-  start_lookup(lane, blk, hg, rq, first, qp, ap);
+  int blk, blk2, hg, rq, first, qp, ap;
+  start_lookup(lane, blk, blk2, hg, rq, first, qp, ap);
   int issued = 0, pieces = 0, cur_piece = -1;
   bool aborted = false;
   for (int g0 = 0; g0 < n && !aborted; g0 += 32) {
-    const int ok = (blk >= 0 && blk < a.num_blocks) ? 1 : 0;
-    if (!ok && g0 + lane < n) report(a.status, KVINJ_ST_BAD_BLOCK);
-    const int row0 = (int)((((int64_t)a.layer * a.num_blocks + (ok ? blk : 0)) * a.Hkv +
+    // valid bits: block 0 (and, with two blocks per unit, block 1) in the cache
+    const int ok0 = (blk >= 0 && blk < a.num_blocks) ? 1 : 0;
+    const int ok1 = (Lay::BPU == 2 && blk2 >= 0 && blk2 < a.num_blocks) ? 2 : 0;
+    if (g0 + lane < n && (!ok0 || (blk2 != -2 && Lay::BPU == 2 && !ok1)))
+      report(a.status, KVINJ_ST_BAD_BLOCK);
+    const int ok = ok0 | ok1;
+    const int row0 = (int)((((int64_t)a.layer * a.num_blocks + (ok0 ? blk : 0)) * a.Hkv +
                             (int64_t)hg * HG) * BLK);
+    const int row1 = (int)((((int64_t)a.layer * a.num_blocks + (ok1 ? blk2 : (ok0 ? blk : 0))) *
+                                a.Hkv + (int64_t)hg * HG) * BLK);
     const int qpos_ok = (qp >= 0 && qp < a.max_pos) ? qp : -1;
     if (Lay::QB && first && a.rope && qpos_ok < 0 && g0 + lane < n) report(a.status, KVINJ_ST_BAD_POS);
     const int qrow0 = rq * a.Hq + hg * HG * Lay::G;  // first q row of the head group
-    int nblk, nhg, nrq, nfirst, nqp, nap;
-    start_lookup(g0 + 32 + lane, nblk, nhg, nrq, nfirst, nqp, nap);
+    int nblk, nblk2, nhg, nrq, nfirst, nqp, nap;
+    start_lookup(g0 + 32 + lane, nblk, nblk2, nhg, nrq, nfirst, nqp, nap);
     const int cnt = min(32, n - g0);
     for (int i = 0; i < cnt; ++i) {
       const int r0 = __shfl_sync(0xffffffffu, row0, i);
+      const int r1 = __shfl_sync(0xffffffffu, row1, i);
       const int oki = __shfl_sync(0xffffffffu, ok, i);
       const int fi = __shfl_sync(0xffffffffu, first, i);
       const int qri = __shfl_sync(0xffffffffu, qrow0, i);
@@ -328,10 +349,25 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
           uint64_t *fb = full + st;
           mbar_arrive_expect_tx(fb, Lay::STAGE_BYTES);
           uint8_t *kd = stages + st * Lay::STAGE_BYTES;
+          if constexpr (Lay::BPU == 1) {
 #pragma unroll
-          for (int b = 0; b < NBOX; ++b) {
-            tma_load_2d(kd + b * Lay::BOXB, &tmK, 64 * b, r0, fb);
-            tma_load_2d(kd + Lay::UNIT_BYTES + b * Lay::BOXB, &tmV, 64 * b, r0, fb);
+            for (int b = 0; b < NBOX; ++b) {
+              tma_load_2d(kd + b * Lay::BOXB, &tmK, 64 * b, r0, fb);
+              tma_load_2d(kd + Lay::UNIT_BYTES + b * Lay::BOXB, &tmV, 64 * b, r0, fb);
+            }
+          } else {
+            // 16-row boxes (one head of one block) placed in (head, block, token) order
+#pragma unroll
+            for (int b = 0; b < NBOX; ++b)
+#pragma unroll
+              for (int h = 0; h < HG; ++h)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                  const int dst = b * Lay::BOXB + (h * 2 + j) * BLK * 128;
+                  const int y = (j ? r1 : r0) + h * BLK;
+                  tma_load_2d(kd + dst, &tmK, 64 * b, y, fb);
+                  tma_load_2d(kd + Lay::UNIT_BYTES + dst, &tmV, 64 * b, y, fb);
+                }
           }
         }
       }
@@ -343,6 +379,7 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
       issued = gi + 1;
     }
     blk = nblk;
+    blk2 = nblk2;
     hg = nhg;
     rq = nrq;
     first = nfirst;
@@ -471,13 +508,13 @@ __device__ void combine_rows(const DecodeArgs &a, const CtaRange &rg, const Piec
 // warp per row over a grid of decode CTAs 42.9 us; this grid of segments: see
 // the design notes.)
 constexpr int COMBINE_WARPS = 8;
-template <int D, int G, int HG, int DT>
+template <int D, int G, int HG, int DT, int BPU>
 __global__ void __launch_bounds__(COMBINE_WARPS * 32) decode_combine_kernel(DecodeArgs a) {
   extern __shared__ int comb_sm[];  // scratch[COMBINE_WARPS], pre[batch + 1]
   int *pre = comb_sm + COMBINE_WARPS;
   const int ngrp = a.Hkv / HG;
   unit_prefix<COMBINE_WARPS * 32>(a, pre, comb_sm,
-                                  [&](int, int c) { return context_pages(a, c) * ngrp; });
+                                  [&](int, int c) { return context_units<BPU>(a, c) * ngrp; });
   CtaRange rg;
   rg.Ptot = pre[a.batch];
   rg.n_eff = min(a.ctas, rg.Ptot);
@@ -532,11 +569,11 @@ cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, c
 }
 
 // the combine pass for a split-K grid of `ctas` CTAs
-template <int D, int G, int HG, int DT>
+template <int D, int G, int HG, int DT, int BPU = 1>
 cudaError_t launch_combine(const DecodeArgs &a, int ctas, cudaStream_t s) {
   DecodeArgs c = a;
   c.ctas = ctas;
-  return launch_pdl(decode_combine_kernel<D, G, HG, DT>,
+  return launch_pdl(decode_combine_kernel<D, G, HG, DT, BPU>,
                     dim3(a.batch * (a.Hkv / HG), (HG * G + COMBINE_WARPS - 1) / COMBINE_WARPS),
                     dim3(COMBINE_WARPS * 32), (size_t)(COMBINE_WARPS + a.batch + 1) * sizeof(int),
                     s, c);

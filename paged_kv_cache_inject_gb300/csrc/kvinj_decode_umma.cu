@@ -10,19 +10,23 @@
 // PagedAttention and the memory-bound Decode Phase).
 //
 // Work split, TMA producer and partial-state protocol are those of
-// kvinj_decode_common.cuh (D = 128, head groups of HG = 8 kv heads: a unit is
-// one block of 8 kv heads, 128 rows of K and 128 rows of V). What differs is
-// the consumer: one MMA per k-step over the whole unit instead of one small
-// contraction per kv head.
+// kvinj_decode_common.cuh (D = 128). A unit is 128 rows of K and 128 rows of
+// V: for G <= 4 one block of a head group of HG = 8 kv heads, for G = 8 two
+// consecutive blocks of a group of HG = 4 kv heads (BPU = 2 blocks per unit),
+// which keeps N = 2*HG*G at 64 so that three stages fit beside the Q and P
+// tiles. What differs from the other kernels is the consumer: one MMA per
+// k-step over the whole unit instead of one small contraction per kv head.
 //
 //   QK: S[128 x N] = K_unit[128 x 128] Q^T[128 x N]. Row i of the unit is
-//       (head i / 16, token i % 16); the N = 16*G columns are, per kv head h
-//       of the group, the hi and the lo 16-bit parts of its G rotated, scaled
-//       queries (columns h*2G + g and h*2G + G + g). Row i only uses the 2G
-//       columns of its own head; the other products are computed and ignored
-//       (the tensor cores have ample slack in this memory-bound loop).
-//   softmax: warps 4..7 each own 32 rows of S (two heads), one row per
-//       thread; the 16 tokens of a head are 16 lanes, reduced with shuffles.
+//       (head i / TPH, token i % TPH of the unit), TPH = 16*BPU; the N columns
+//       are, per kv head h of the group, the hi and the lo 16-bit parts of its
+//       G rotated, scaled queries (columns h*2G + g and h*2G + G + g). Row i
+//       only uses the 2G columns of its own head; the other products are
+//       computed and ignored (the tensor cores have ample slack in this
+//       memory-bound loop).
+//   softmax: warps 4..7 each own 32 rows of S (two heads, or one at G = 8),
+//       one row per thread; a head's tokens are TPH lanes, reduced with
+//       shuffles.
 //   PV: O^T[128 x N] += V_unit^T[128 x 128] P^T[128 x N], where P^T is block
 //       diagonal: the column of query head (h, g) holds that head's 16
 //       probabilities in the rows of head h and zeros elsewhere, so each
@@ -57,9 +61,10 @@ namespace kvinj {
 
 constexpr float UMMA_TAU = 8.f;  // lazy-maximum threshold, log2 units
 
-template <int G_, int S_, int QBUF_>
+template <int G_, int S_, int QBUF_, int HG_ = 8, int BPU_ = 1>
 struct UmmaLayout {
-  static constexpr int D = 128, G = G_, HG = 8, S = S_;
+  static constexpr int D = 128, G = G_, HG = HG_, S = S_;
+  static constexpr int BPU = BPU_;           // 16-token blocks per unit (HG*BPU*16 = 128 rows)
   static constexpr int QB = 0;               // the producer stages no query rows
   static constexpr int QBUF = QBUF_;         // Q tiles, written by the query warps
   static constexpr int EMPTY_ARRIVALS = 1;   // one MMA commit frees a stage
@@ -67,7 +72,7 @@ struct UmmaLayout {
   static constexpr bool APPEND_WAIT = true;  // the producer waits for a fused append
   static constexpr int N = HG * 2 * G;       // MMA N
   static constexpr int NBOX = D / 64;
-  static constexpr int BOXB = HG * BLK * 128;          // 16 KiB
+  static constexpr int BOXB = HG * BPU * BLK * 128;    // 16 KiB: 128 rows of 128 bytes
   static constexpr int UNIT_BYTES = NBOX * BOXB;       // 32 KiB of K (or V)
   static constexpr int STAGE_BYTES = 2 * UNIT_BYTES;
   static constexpr int TILE_BYTES = N * 2 * D;         // N rows x 128 elements
@@ -95,6 +100,7 @@ struct UmmaLayout {
   // bytes saved let a combine CTA stay resident beside this one)
   static size_t bytes(int batch) { return (size_t)off_pre + (size_t)(2 * batch + 1) * 4; }
   static_assert(3 * N <= 512, "tensor memory: S[2] and O");
+  static_assert(HG * BPU * BLK == 128, "a unit is 128 rows: the MMA's M");
   static_assert(off_q % 1024 == 0 && off_p % 1024 == 0, "swizzle atoms are 1024-byte aligned");
 };
 
@@ -115,12 +121,14 @@ __device__ __forceinline__ void sts128_zero(uint32_t addr) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
 }
 
-template <int G, int S, int QBUF, int DT>
+template <int G, int S, int QBUF, int DT, int HG = 8, int BPU = 1>
 __global__ void __launch_bounds__(256, 1)
     decode_umma_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, DecodeArgs a) {
-  using Lay = UmmaLayout<G, S, QBUF>;
-  constexpr int D = 128, HG = 8, N = Lay::N, PF = partial_floats(G, D), SLOT = HG * PF;
+  using Lay = UmmaLayout<G, S, QBUF, HG, BPU>;
+  constexpr int D = 128, N = Lay::N, PF = partial_floats(G, D), SLOT = HG * PF;
+  constexpr int TPH = BLK * BPU;   // tokens of a head in a unit (its rows are consecutive)
+  constexpr int HPW = 32 / TPH;    // heads per softmax warp
   static_assert(G == 1 || G == 2 || G == 4 || G == 8, "tcgen05 decode: G");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -224,7 +232,7 @@ __global__ void __launch_bounds__(256, 1)
           tc_fence_after();
           const uint32_t vb = stage0 + st * Lay::STAGE_BYTES + Lay::UNIT_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < HG * BLK / 16; ++kk)
+          for (int kk = 0; kk < HG * BPU * BLK / 16; ++kk)
             umma_f16(tbase + 2 * N, umma_desc_sw128(vb + kk * 2048, Lay::BOXB, 1024),
                      umma_desc_sw128(p0 + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024),
                      ID_PV, (j > 0 || kk > 0) ? 1u : 0u);
@@ -275,9 +283,9 @@ __global__ void __launch_bounds__(256, 1)
       // fused append: the token at q_pos, if its block is one of this piece's
       // units, is written here (K rotated at q_pos with the same table row)
       const int qa = qpos_sm[pc.r];
-      const int pg_a = qa >= 0 ? qa / BLK : -1;
-      const bool app = a.k_new && qa >= 0 && (!a.rope || qa < a.max_pos) && pg_a >= pc.pg0 &&
-                       pg_a < pc.pg0 + (pc.end - P);
+      const int pg_a = qa >= 0 ? qa / BLK : -1;  // the block of the new token
+      const bool app = a.k_new && qa >= 0 && (!a.rope || qa < a.max_pos) &&
+                       pg_a / BPU >= pc.pg0 && pg_a / BPU < pc.pg0 + (pc.end - P);
       uint32_t akx[HG / 2], aky[HG / 2], avx[HG / 2], avy[HG / 2];
       int64_t abl = -1;
       if (app) {
@@ -356,7 +364,8 @@ __global__ void __launch_bounds__(256, 1)
     // -------------------------------- softmax --------------------------------
     const int qd = warp & 3;            // TMEM lane quadrant
     const int row = 32 * qd + lane;     // unit row = head * 16 + token; O row = dimension
-    const int hs = lane >> 4, h = 2 * qd + hs, t = lane & 15;
+    // unit row = (head, token of the unit): head h owns rows TPH*h .. TPH*h + TPH-1
+    const int hs = lane / TPH, h = HPW * qd + hs, t = lane % TPH;
     float *alpha_sm = reinterpret_cast<float *>(sm + Lay::off_alpha);
     volatile int *rflag = reinterpret_cast<volatile int *>(alpha_sm + 2 * N);
     float *m_sm = reinterpret_cast<float *>(sm + Lay::off_ml), *l_sm = m_sm + HG * G;
@@ -379,22 +388,24 @@ __global__ void __launch_bounds__(256, 1)
         const int gi = gi0 + j, st = gi % S, par = gi & 1;
         const bool ok = wait(full + st, (uint32_t)(gi / S) & 1u) &&
                         wait(sfull + par, (uint32_t)(gi >> 1) & 1u);
-        int nv = 0;
-        if (ok && valid[st]) nv = max(0, min(BLK, pc.ctx - (pc.pg0 + j) * BLK));
+        // this thread's token: in the context and in a block the cache holds
+        const bool live = ok && ((valid[st] >> (t / BLK)) & 1) &&
+                          (pc.pg0 + j) * TPH + t < pc.ctx;
         float s[G];
         if (ok) {
           tc_fence_after();
-          uint32_t r[4 * G];
-          tmem_ld<4 * G>(tmem_addr(tbase + par * N, 32 * qd, 4 * G * qd), r);
+          uint32_t r[HPW * 2 * G];
+          tmem_ld<HPW * 2 * G>(tmem_addr(tbase + par * N, 32 * qd, HPW * 2 * G * qd), r);
 #pragma unroll
           for (int g = 0; g < G; ++g)
-            s[g] = hs ? __uint_as_float(r[2 * G + g]) + __uint_as_float(r[3 * G + g])
-                      : __uint_as_float(r[g]) + __uint_as_float(r[G + g]);
+            s[g] = (HPW == 2 && hs) ? __uint_as_float(r[(2 * G + g) % (HPW * 2 * G)]) +
+                                          __uint_as_float(r[(3 * G + g) % (HPW * 2 * G)])
+                                    : __uint_as_float(r[g]) + __uint_as_float(r[G + g]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(sfree + par);
-        if (t >= nv) {
+        if (!live) {
 #pragma unroll
           for (int g = 0; g < G; ++g) s[g] = -INFINITY;
         }
@@ -404,10 +415,8 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           float mu = s[g];
-          mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, 1));
-          mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, 2));
-          mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, 4));
-          mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, 8));
+#pragma unroll
+          for (int o = 1; o < TPH; o <<= 1) mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, o));
           alpha[g] = 1.f;
           if (mu > m_run[g] + UMMA_TAU) {  // also the first finite maximum
             alpha[g] = exp2f(m_run[g] - mu);
@@ -460,7 +469,7 @@ __global__ void __launch_bounds__(256, 1)
         }
         // V rows past the context may hold anything (even NaN bit patterns):
         // zero them so that 0 * V stays 0
-        if (t >= nv) {
+        if (!live) {
           const uint32_t vr = stage0 + st * Lay::STAGE_BYTES + Lay::UNIT_BYTES + row * 128;
 #pragma unroll
           for (int b = 0; b < Lay::NBOX; ++b)
@@ -478,10 +487,8 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float x = l_part[g];
-        x += __shfl_xor_sync(0xffffffffu, x, 1);
-        x += __shfl_xor_sync(0xffffffffu, x, 2);
-        x += __shfl_xor_sync(0xffffffffu, x, 4);
-        x += __shfl_xor_sync(0xffffffffu, x, 8);
+#pragma unroll
+        for (int o = 1; o < TPH; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
         l_tot[g] = x;
       }
       if (t == 0) {
@@ -534,11 +541,11 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
-template <int G, int S, int QBUF, int DT>
+template <int G, int S, int QBUF, int DT, int HG, int BPU>
 static cudaError_t launch_umma_cfg(const DecodeArgs &a, const CUtensorMap &tmK,
                                    const CUtensorMap &tmV, int ctas, cudaStream_t s) {
-  auto kern = decode_umma_kernel<G, S, QBUF, DT>;
-  const size_t smem = UmmaLayout<G, S, QBUF>::bytes(a.batch);
+  auto kern = decode_umma_kernel<G, S, QBUF, DT, HG, BPU>;
+  const size_t smem = UmmaLayout<G, S, QBUF, HG, BPU>::bytes(a.batch);
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -548,19 +555,22 @@ static cudaError_t launch_umma_cfg(const DecodeArgs &a, const CUtensorMap &tmK,
   }
   cudaError_t e = launch_pdl(kern, dim3(ctas), dim3(256), smem, s, tmK, tmV, a);
   if (e != cudaSuccess) return e;
-  return launch_combine<128, G, 8, DT>(a, ctas, s);
+  return launch_combine<128, G, HG, DT, BPU>(a, ctas, s);
 }
 
-// three stages when they fit beside the Q and P tiles, else two
+// three stages when they fit beside the Q and P tiles, else two. G = 8 takes units of two
+// blocks of 4 kv heads (N = 64: the tiles of G = 4, three stages) instead of one block of 8
+// (N = 128: two stages).
 template <int G, int DT>
 static cudaError_t launch_umma(const DecodeArgs &a, const CUtensorMap &tmK,
                                const CUtensorMap &tmV, int ctas, cudaStream_t s) {
-  if (UmmaLayout<G, 3, 2>::bytes(a.batch) <= (size_t)DECODE_MAX_SMEM)
-    return launch_umma_cfg<G, 3, 2, DT>(a, tmK, tmV, ctas, s);
-  if (UmmaLayout<G, 3, 1>::bytes(a.batch) <= (size_t)DECODE_MAX_SMEM)
-    return launch_umma_cfg<G, 3, 1, DT>(a, tmK, tmV, ctas, s);
-  if (UmmaLayout<G, 2, 1>::bytes(a.batch) <= (size_t)DECODE_MAX_SMEM)
-    return launch_umma_cfg<G, 2, 1, DT>(a, tmK, tmV, ctas, s);
+  constexpr int HG = G == 8 ? 4 : 8, BPU = G == 8 ? 2 : 1;
+  if (UmmaLayout<G, 3, 2, HG, BPU>::bytes(a.batch) <= (size_t)DECODE_MAX_SMEM)
+    return launch_umma_cfg<G, 3, 2, DT, HG, BPU>(a, tmK, tmV, ctas, s);
+  if (UmmaLayout<G, 3, 1, HG, BPU>::bytes(a.batch) <= (size_t)DECODE_MAX_SMEM)
+    return launch_umma_cfg<G, 3, 1, DT, HG, BPU>(a, tmK, tmV, ctas, s);
+  if (UmmaLayout<G, 2, 1, HG, BPU>::bytes(a.batch) <= (size_t)DECODE_MAX_SMEM)
+    return launch_umma_cfg<G, 2, 1, DT, HG, BPU>(a, tmK, tmV, ctas, s);
   return cudaErrorInvalidValue;
 }
 

@@ -97,7 +97,7 @@ class Engine:
     def uses_tcgen05(self) -> bool:
         """Whether decode runs the tcgen05 kernel (one launch per layer)."""
         G = self.Hq // self.Hkv
-        ok = self.D == 128 and self.Hkv % 8 == 0 and G in (1, 2, 4)  # the automatic choice
+        ok = self.D == 128 and self.Hkv % 8 == 0 and G in (1, 2, 4, 8)  # the automatic choice
         return self.decode_variant == 3 or (self.decode_variant == 0 and ok)
 
     def launches_per_layer(self) -> int:

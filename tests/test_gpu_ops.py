@@ -396,8 +396,10 @@ def test_decode_umma_large_logits_move_the_maximum(scale, G):
         assert_decode_close(got, want, f"umma scale{scale} G{G} ctas{ctas}")
 
 
-def test_decode_umma_long_context_unrotated_and_bad_inputs():
-    D, G, dt = 128, 4, W.BF16
+@pytest.mark.parametrize("G", [4, 8])
+def test_decode_umma_long_context_unrotated_and_bad_inputs(G):
+    # at G = 8 a unit spans two blocks: a bad entry in either half is caught
+    D, dt = 128, W.BF16
     ctx = np.array([9000, 3, 4097], np.int32)
     kc, vc, q, bt = _decode_case(D, G, dt, ctx, Hkv=8, L=1, seed=61)
     got, _ = _run_decode(kc, vc, q, bt, ctx, ctx - 1, dt, 0, 5e5, 9000, variant=3)
@@ -415,20 +417,25 @@ def test_decode_umma_long_context_unrotated_and_bad_inputs():
     assert not got[0].any() and not got[2].any()
     want, _ = oracle.paged_decode(kc, vc, 0, q[1:2], [2], bt[1:2], [3], 5e5, dt)
     assert_decode_close(got[1:2], want, "umma valid request next to invalid ones")
-    bt2 = bt.copy()
-    bt2[0, 5] = kc.shape[1] + 7  # a block-table entry outside the cache
-    status = status_tensor()
-    got, _ = _run_decode(kc, vc, q, bt2, ctx, ctx - 1, dt, 0, 5e5, 9000, status=status, variant=3)
-    assert status.item() == K.ST_BAD_BLOCK
-    want, _ = oracle.paged_decode(kc, vc, 0, q[1:], ctx[1:] - 1, bt[1:], ctx[1:], 5e5, dt)
-    assert_decode_close(got[1:], want, "umma requests after a bad block")
+    for idx in (4, 5):
+        bt2 = bt.copy()
+        bt2[0, idx] = kc.shape[1] + 7  # a block-table entry outside the cache
+        status = status_tensor()
+        got, _ = _run_decode(kc, vc, q, bt2, ctx, ctx - 1, dt, 0, 5e5, 9000, status=status,
+                             variant=3)
+        assert status.item() == K.ST_BAD_BLOCK
+        want, _ = oracle.paged_decode(kc, vc, 0, q[1:], ctx[1:] - 1, bt[1:], ctx[1:], 5e5, dt)
+        assert_decode_close(got[1:], want, f"umma requests after bad block {idx}")
 
 
 @pytest.mark.parametrize("variant", [1, 2, 3])
-def test_decode_ignores_nan_rows_past_the_context(variant):
+@pytest.mark.parametrize("G", [4, 8])
+def test_decode_ignores_nan_rows_past_the_context(variant, G):
     # rows of a request's last block past its context may hold anything; NaN
-    # bit patterns there must not reach the output
-    D, G, dt, Hkv = 128, 4, W.BF16, 8
+    # bit patterns there must not reach the output (at G = 8 the tcgen05 kernel's
+    # units span two blocks: also the second block's rows of a unit the context
+    # ends before, e.g. 7 or 16 tokens)
+    D, dt, Hkv = 128, W.BF16, 8
     ctx = np.array([33, 250, 7, 16], np.int32)
     kc, vc, q, bt = _decode_case(D, G, dt, ctx, Hkv=Hkv, L=2, seed=71)
     for r, c in enumerate(ctx):
@@ -439,7 +446,7 @@ def test_decode_ignores_nan_rows_past_the_context(variant):
     got, _ = _run_decode(kc, vc, q, bt, ctx, ctx - 1, dt, 1, 5e5, 300, variant=variant)
     assert np.isfinite(got).all()
     want, _ = oracle.paged_decode(kc, vc, 1, q, ctx - 1, bt, ctx, 5e5, dt)
-    assert_decode_close(got, want, f"nan tail variant{variant}")
+    assert_decode_close(got, want, f"nan tail variant{variant} G{G}")
 
 
 def test_decode_umma_refuses_shapes_it_does_not_cover():
@@ -504,8 +511,9 @@ def test_append_paged_decode_matches_oracle(variant, ctas, G, Hkv):
     assert_decode_close(got, want, f"fused variant{variant} ctas{ctas} G{G} Hkv{Hkv}")
 
 
-def test_append_paged_decode_equals_separate_calls_bitwise():
-    D, G, dt, Hkv = 128, 4, W.BF16, 8
+@pytest.mark.parametrize("G", [4, 8])
+def test_append_paged_decode_equals_separate_calls_bitwise(G):
+    D, dt, Hkv = 128, W.BF16, 8
     ctx = [700, 33, 1500, 16, 2048, 5]
     kc, vc, q, bt, kn, vn, ctx, pos, slots, theta, ek, ev, want = _fused_case(
         D, G, dt, ctx, Hkv, seed=97)
