@@ -41,6 +41,8 @@ struct DecodeLayout {
   static constexpr bool QPOS_SM = false;  // q positions copied to shared memory after pre[]
   static constexpr bool APPEND_WAIT = false;  // the producer waits for a fused append
   static constexpr int BPU = 1;               // 16-token blocks per unit
+  static constexpr bool SPLIT_KV = false;     // K and V of a stage share one barrier pair
+  static constexpr int VR = S;                // valid bits: one entry per stage
   static constexpr int off_qfull = 0, QBUF = 1;
   static constexpr int NBOX = D / 64;                   // 64-element (128-byte) column boxes
   static constexpr int BOXB = HG * BLK * 128;           // bytes of one box: HG*16 rows
@@ -210,6 +212,13 @@ __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) 
       mbar_init(full + 2 * Lay::S + b, 1);
       mbar_init(full + 2 * Lay::S + Lay::QB + b, Lay::HG);
     }
+    if constexpr (Lay::SPLIT_KV) {
+      static_assert(Lay::QB == 0, "split stages: the producer stages no query rows");
+      for (int s = 0; s < Lay::S; ++s) {
+        mbar_init(full + 2 * Lay::S + s, 1);                    // V landed
+        mbar_init(full + 3 * Lay::S + s, Lay::EMPTY_ARRIVALS);  // V released
+      }
+    }
     flags[0] = 0;
     flags[1] = 0;
     fence_mbar_init();
@@ -228,6 +237,8 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
   constexpr int S = Lay::S, NBOX = Lay::NBOX, HG = Lay::HG;
   uint64_t *full = reinterpret_cast<uint64_t *>(sm + Lay::off_bar);
   uint64_t *empty = full + S;
+  // split stages: full/empty cover the K half, fullV/emptyV the V half
+  uint64_t *fullV = full + 2 * S, *emptyV = full + 3 * S;
   volatile int *flags = reinterpret_cast<volatile int *>(sm + Lay::off_flags);
   int *valid = reinterpret_cast<int *>(sm + Lay::off_valid);
   const int *pre = reinterpret_cast<const int *>(sm + Lay::off_pre);
@@ -275,7 +286,8 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
   };
   int blk, blk2, hg, rq, first, qp, ap;
   start_lookup(lane, blk, blk2, hg, rq, first, qp, ap);
-  int issued = 0, pieces = 0, cur_piece = -1;
+  int pieces = 0, cur_piece = -1;
+  int kiss = 0, viss = 0;  // (lane 0) units whose K (V) copies were issued
   bool aborted = false;
   for (int g0 = 0; g0 < n && !aborted; g0 += 32) {
     // valid bits: block 0 (and, with two blocks per unit, block 1) in the cache
@@ -345,29 +357,44 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
           go = 0;
         }
         if (go) {
-          valid[st] = oki;
-          uint64_t *fb = full + st;
-          mbar_arrive_expect_tx(fb, Lay::STAGE_BYTES);
+          valid[Lay::SPLIT_KV ? gi % Lay::VR : st] = oki;
           uint8_t *kd = stages + st * Lay::STAGE_BYTES;
-          if constexpr (Lay::BPU == 1) {
+          // the boxes of one tensor (K or V) of this unit into dst, counted on bar
+          auto load_half = [&](uint8_t *dst, const CUtensorMap *tm, uint64_t *bar) {
+            if constexpr (Lay::BPU == 1) {
 #pragma unroll
-            for (int b = 0; b < NBOX; ++b) {
-              tma_load_2d(kd + b * Lay::BOXB, &tmK, 64 * b, r0, fb);
-              tma_load_2d(kd + Lay::UNIT_BYTES + b * Lay::BOXB, &tmV, 64 * b, r0, fb);
+              for (int b = 0; b < NBOX; ++b) tma_load_2d(dst + b * Lay::BOXB, tm, 64 * b, r0, bar);
+            } else {
+              // 16-row boxes (one head of one block) placed in (head, block, token) order
+#pragma unroll
+              for (int b = 0; b < NBOX; ++b)
+#pragma unroll
+                for (int h = 0; h < HG; ++h)
+#pragma unroll
+                  for (int j = 0; j < 2; ++j)
+                    tma_load_2d(dst + b * Lay::BOXB + (h * 2 + j) * BLK * 128, tm, 64 * b,
+                                (j ? r1 : r0) + h * BLK, bar);
+            }
+          };
+          if constexpr (Lay::SPLIT_KV) {
+            // K is released once its QK is done, V once its PV is: K runs ahead of V
+            mbar_arrive_expect_tx(full + st, Lay::UNIT_BYTES);
+            load_half(kd, &tmK, full + st);
+            kiss = gi + 1;
+            if (gi >= S && !mbar_wait_bounded(emptyV + st, (uint32_t)(gi / S - 1) & 1u)) {
+              report(a.status, KVINJ_ST_TIMEOUT);
+              flags[0] = 1;
+              go = 0;
+            } else {
+              mbar_arrive_expect_tx(fullV + st, Lay::UNIT_BYTES);
+              load_half(kd + Lay::UNIT_BYTES, &tmV, fullV + st);
+              viss = gi + 1;
             }
           } else {
-            // 16-row boxes (one head of one block) placed in (head, block, token) order
-#pragma unroll
-            for (int b = 0; b < NBOX; ++b)
-#pragma unroll
-              for (int h = 0; h < HG; ++h)
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                  const int dst = b * Lay::BOXB + (h * 2 + j) * BLK * 128;
-                  const int y = (j ? r1 : r0) + h * BLK;
-                  tma_load_2d(kd + dst, &tmK, 64 * b, y, fb);
-                  tma_load_2d(kd + Lay::UNIT_BYTES + dst, &tmV, 64 * b, y, fb);
-                }
+            mbar_arrive_expect_tx(full + st, Lay::STAGE_BYTES);
+            load_half(kd, &tmK, full + st);
+            load_half(kd + Lay::UNIT_BYTES, &tmV, full + st);
+            kiss = viss = gi + 1;
           }
         }
       }
@@ -376,7 +403,6 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
         aborted = true;
         break;
       }
-      issued = gi + 1;
     }
     blk = nblk;
     blk2 = nblk2;
@@ -388,8 +414,11 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
   }
   if (aborted && lane == 0) {
     // let the copies already in flight land before the CTA can exit
-    for (int gi = max(0, issued - S); gi < issued; ++gi)
+    for (int gi = max(0, kiss - S); gi < kiss; ++gi)
       mbar_wait_bounded(full + gi % S, (uint32_t)(gi / S) & 1u, 100000000ull);
+    if constexpr (Lay::SPLIT_KV)
+      for (int gi = max(0, viss - S); gi < viss; ++gi)
+        mbar_wait_bounded(fullV + gi % S, (uint32_t)(gi / S) & 1u, 100000000ull);
     for (int k = max(0, pieces - Lay::QB); k < pieces; ++k)
       mbar_wait_bounded(full + 2 * S + k % (Lay::QB ? Lay::QB : 1), (uint32_t)(k / (Lay::QB ? Lay::QB : 1)) & 1u,
                         100000000ull);

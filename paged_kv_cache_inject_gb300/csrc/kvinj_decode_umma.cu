@@ -67,7 +67,14 @@ struct UmmaLayout {
   static constexpr int BPU = BPU_;           // 16-token blocks per unit (HG*BPU*16 = 128 rows)
   static constexpr int QB = 0;               // the producer stages no query rows
   static constexpr int QBUF = QBUF_;         // Q tiles, written by the query warps
-  static constexpr int EMPTY_ARRIVALS = 1;   // one MMA commit frees a stage
+  static constexpr int EMPTY_ARRIVALS = 1;   // one MMA commit frees a stage half
+  // two-block units (G = 8): K and V halves of a stage have their own barriers, K is freed
+  // after its QK and V after its PV (measured faster there; one-block units keep one pair)
+  static constexpr bool SPLIT_KV = BPU == 2;
+  // valid bits of each unit's blocks: one entry per stage; split stages keep them in a
+  // ring, as unit gi's entry is written when its K is issued (after QK(gi - S)), when the
+  // softmax has read the entries of units up to gi - S - 2
+  static constexpr int VR = SPLIT_KV ? 8 : S;
   static constexpr bool QPOS_SM = true;      // the query warps read q positions there
   static constexpr bool APPEND_WAIT = true;  // the producer waits for a fused append
   static constexpr int N = HG * 2 * G;       // MMA N
@@ -81,15 +88,16 @@ struct UmmaLayout {
   static constexpr int off_q = S * STAGE_BYTES;        // [QBUF] Q tiles
   static constexpr int off_t = off_q;                  // unused
   static constexpr int off_p = off_q + QBUF * TILE_BYTES;
-  static constexpr int off_bar = off_p + TILE_BYTES;   // full[S], empty[S]
+  static constexpr int off_bar = off_p + TILE_BYTES;   // full[S] empty[S] (K), fullV[S] emptyV[S]
+                                                       // (split stages; else full/empty cover both)
   // sfull[2] sfree[2] pfull pvdone qfull[QBUF] qempty[QBUF] ofree done
   static constexpr int NXBAR = 8 + 2 * QBUF;
-  static constexpr int off_xbar = off_bar + 2 * S * 8;
+  static constexpr int off_xbar = off_bar + (SPLIT_KV ? 4 : 2) * S * 8;
   static constexpr int off_qfull = off_xbar + 6 * 8;  // qfull[QBUF] (see below)
-  static constexpr int off_valid = off_xbar + NXBAR * 8;
-  static constexpr int off_qinfo = off_valid + S * 4;  // unused
-  static constexpr int off_flags = off_qinfo + 16;
-  static constexpr int off_alpha = off_flags + 256;    // [2][N] factors, [2][4] flags
+  static constexpr int off_valid = off_xbar + NXBAR * 8;  // [VR] valid bits
+  static constexpr int off_qinfo = off_valid + VR * 4;  // unused (no bytes)
+  static constexpr int off_flags = off_qinfo;          // [0] abort [1] unused [8..16) scan
+  static constexpr int off_alpha = off_flags + 64;     // [2][N] factors, [2][4] flags
   static constexpr int off_ml = off_alpha + 2 * N * 4 + 32;
   static constexpr int off_tmem = off_ml + 2 * HG * G * 4;
   static constexpr int off_pre = off_tmem + 16;        // pre[batch + 1], then qpos[batch]
@@ -139,8 +147,9 @@ __global__ void __launch_bounds__(256, 1)
     return;
   }
 
-  uint64_t *full = reinterpret_cast<uint64_t *>(sm + Lay::off_bar);
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm + Lay::off_bar);  // K halves of the stages
   uint64_t *empty = full + S;
+  uint64_t *fullV = full + 2 * S, *emptyV = full + 3 * S;             // V halves
   uint64_t *sfull = reinterpret_cast<uint64_t *>(sm + Lay::off_xbar);
   uint64_t *sfree = sfull + 2, *pfull = sfull + 4, *pvdone = sfull + 5;
   uint64_t *qfull = sfull + 6, *qempty = qfull + QBUF, *ofree = qempty + QBUF, *done = ofree + 1;
@@ -210,6 +219,7 @@ __global__ void __launch_bounds__(256, 1)
                    umma_desc_sw128(qb + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024), ID_QK,
                    kk > 0);
         umma_commit(sfull + (gi & 1));
+        if constexpr (Lay::SPLIT_KV) umma_commit(empty + st);  // the K half is free
       };
       int P = rg.b0, gi0 = 0, piece = 0;
       while (P < rg.b1) {
@@ -229,6 +239,7 @@ __global__ void __launch_bounds__(256, 1)
           }
           if (j + 1 >= np) umma_commit(qempty + qbuf);  // the Q tile is free once its QKs are done
           if (!wait(pfull, (uint32_t)gi & 1u)) continue;
+          if (Lay::SPLIT_KV && !wait(fullV + st, (uint32_t)(gi / S) & 1u)) continue;
           tc_fence_after();
           const uint32_t vb = stage0 + st * Lay::STAGE_BYTES + Lay::UNIT_BYTES;
 #pragma unroll
@@ -236,7 +247,7 @@ __global__ void __launch_bounds__(256, 1)
             umma_f16(tbase + 2 * N, umma_desc_sw128(vb + kk * 2048, Lay::BOXB, 1024),
                      umma_desc_sw128(p0 + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024),
                      ID_PV, (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(empty + st);
+          umma_commit(Lay::SPLIT_KV ? emptyV + st : empty + st);
           umma_commit(pvdone);
           if (!qk_next) issue_qk(gi + 1, qbuf);
         }
@@ -386,10 +397,14 @@ __global__ void __launch_bounds__(256, 1)
       }
       for (int j = 0; j < np; ++j) {
         const int gi = gi0 + j, st = gi % S, par = gi & 1;
-        const bool ok = wait(full + st, (uint32_t)(gi / S) & 1u) &&
+        // the stage's V rows and S. With split stages the wait is on the V half: the K
+        // half is released after its QK and its barrier may already be phases ahead, while
+        // V is held until this unit's PV (the producer writes the valid bits before it
+        // issues the V half).
+        const bool ok = wait((Lay::SPLIT_KV ? fullV : full) + st, (uint32_t)(gi / S) & 1u) &&
                         wait(sfull + par, (uint32_t)(gi >> 1) & 1u);
         // this thread's token: in the context and in a block the cache holds
-        const bool live = ok && ((valid[st] >> (t / BLK)) & 1) &&
+        const bool live = ok && ((valid[Lay::SPLIT_KV ? gi % Lay::VR : st] >> (t / BLK)) & 1) &&
                           (pc.pg0 + j) * TPH + t < pc.ctx;
         float s[G];
         if (ok) {
