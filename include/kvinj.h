@@ -95,13 +95,18 @@ typedef struct {
 } kvinj_cache;
 
 /* resident pool of pre-RoPE memory chunks ("facts"), one contiguous record
- * of 2*L*chunk_len*Hkv*D elements per chunk (InferScale §3.4) */
+ * of 2*L*chunk_len*Hkv*D elements per chunk (InferScale §3.4). The pool may
+ * also live in page-locked host memory (InferScale §6.7, Table 6: the store
+ * kept in pinned host DRAM when GPU memory cannot hold it): the inject kernel
+ * then reads the records in place over the host link (no staging copy). */
 typedef struct {
   int32_t num_layers, num_kv_heads, head_dim;
   int32_t chunk_len;  /* c: tokens per chunk */
   int64_t num_chunks; /* records in the pool */
   int32_t dtype;
-  const void *data; /* device [num_chunks][L][2][c][Hkv][D] */
+  const void *data; /* [num_chunks][L][2][c][Hkv][D]: device memory, or host
+                       memory page-locked with cudaHostAlloc / cudaHostRegister
+                       (mapped); other host memory is refused (KVINJ_EINVAL) */
 } kvinj_pool;
 
 /* RoPE table on the device (layout in the header comment) */
@@ -139,7 +144,10 @@ int kvinj_slot_mapping(const int32_t *block_tables, int32_t max_blocks, int32_t 
  * arithmetic with the fp64-derived table, rounded once, nearest-even) and
  * written to k[l][slot / B][h][slot % B][:], its V row is copied bit for bit
  * to v. Pool and cache must agree in L, Hkv, D and dtype; rope->head_dim ==
- * D. Chunks that overlap in slots race (undefined which one wins). */
+ * D. Chunks that overlap in slots race (undefined which one wins). A pool in
+ * page-locked host memory gives the same results; the call reads it through
+ * its device mapping. KVINJ_EINVAL when pool->data is neither device memory
+ * nor page-locked host memory mapped into the device's address space. */
 int kvinj_inject(const kvinj_pool *pool, const kvinj_cache *cache, const kvinj_rope *rope,
                  const int32_t *chunk_ids, const int32_t *start_pos,
                  const int64_t *slot_mapping, int32_t n_inj, int32_t layer_begin,

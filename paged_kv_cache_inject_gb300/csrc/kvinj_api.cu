@@ -43,6 +43,20 @@ namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// The address under which the device reads p: p itself for device memory, the mapped
+// address of page-locked host memory, nullptr for anything else (pageable host memory,
+// an unknown pointer).
+const void *device_view(const void *p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // the failed query's error is not sticky: clear it
+    return nullptr;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return p;
+  if (at.type == cudaMemoryTypeHost) return at.devicePointer;
+  return nullptr;
+}
+
 bool dtype_ok(int dt) { return dt == KVINJ_BF16 || dt == KVINJ_FP16; }
 
 int check_cache(const kvinj_cache *c, bool decode) {
@@ -165,8 +179,11 @@ int kvinj_inject(const kvinj_pool *pool, const kvinj_cache *cache, const kvinj_r
     return KVINJ_EINVAL;
   if (n_inj == 0 || layer_begin == layer_end) return KVINJ_OK;
   if (!chunk_ids || !start_pos || !slot_mapping) return KVINJ_EINVAL;
+  // device memory, or page-locked host memory read in place over the host link
+  const void *pool_dev = device_view(pool->data);
+  if (!pool_dev || !aligned16(pool_dev)) return KVINJ_EINVAL;
   InjectArgs a;
-  a.pool = static_cast<const uint16_t *>(pool->data);
+  a.pool = static_cast<const uint16_t *>(pool_dev);
   a.L = cache->num_layers;
   a.Hkv = cache->num_kv_heads;
   a.chunk_len = pool->chunk_len;

@@ -132,10 +132,12 @@ class Cache:
 
 
 class Pool:
-    """Pre-RoPE chunk pool: data [num_chunks][L][2][chunk_len][Hkv][D] on the GPU."""
+    """Pre-RoPE chunk pool: data [num_chunks][L][2][chunk_len][Hkv][D] on the GPU, or in
+    page-locked host memory (a pinned CPU tensor), which inject reads in place."""
 
     def __init__(self, data: torch.Tensor):
-        assert data.dim() == 6 and data.shape[2] == 2 and data.is_cuda and data.is_contiguous()
+        assert data.dim() == 6 and data.shape[2] == 2 and data.is_contiguous()
+        assert data.is_cuda or data.is_pinned(), "the pool is device or pinned host memory"
         n, L, _, c, Hkv, D = data.shape
         self.data = data
         self._s = _Pool(L, Hkv, D, c, n, _dtype_code(data.dtype), data.data_ptr())

@@ -4,6 +4,8 @@ edge cases (empty, ragged, single token, invalid indices, workspace size).
 
 Inputs come from the shared seeded generator (workload); expectations only
 from oracle/. Calls go through the C ABI (ctypes binding)."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -158,6 +160,70 @@ def test_inject_layer_range_and_bad_indices():
     assert np.array_equal(gv, vc)
     assert ulp_distance(gk, kc).max() <= 1
     assert np.all(gk[0] == SENTINEL) and np.all(gk[2] == SENTINEL)
+
+
+@pytest.mark.parametrize("D,dt", [(128, W.BF16), (64, W.FP16)])
+def test_inject_from_pinned_host_pool(D, dt):
+    # the chunk pool kept in page-locked host memory ("InferScale" §6.7, Table 6) and read
+    # in place: the same cache bits as with the pool in device memory, within one ulp of
+    # the oracle for rotated K, V copied exactly
+    cs = _inject_case(D, dt, seed=11)
+    L, Hkv, B, NB = cs["L"], cs["Hkv"], cs["B"], cs["NB"]
+    tdt = torch_dtype(dt)
+    theta = 5e5
+    kc = np.full((L, NB, Hkv, B, D), SENTINEL, np.uint16)
+    vc = kc.copy()
+    assert oracle.inject(cs["pool"], cs["ids"], cs["start"], cs["slots"], theta, dt, kc, vc) == 0
+    rope = K.make_rope(theta, D, 200)
+    slots_d = torch.from_numpy(cs["slots"]).cuda()
+    got = {}
+    for where in ("device", "host"):
+        data = from_bits(cs["pool"], tdt)
+        if where == "host":
+            data = data.cpu().pin_memory()
+            assert not data.is_cuda and data.is_pinned()
+        cache = K.Cache(from_bits(np.full_like(kc, SENTINEL), tdt),
+                        from_bits(np.full_like(kc, SENTINEL), tdt))
+        status = status_tensor()
+        K.kvinj_inject(K.Pool(data), cache, rope, i32(cs["ids"]), i32(cs["start"]), slots_d,
+                       status=status)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        got[where] = (bits(cache.k), bits(cache.v))
+    (dk, dv), (hk, hv) = got["device"], got["host"]
+    assert np.array_equal(hk, dk) and np.array_equal(hv, dv)
+    assert np.array_equal(hv, vc)
+    written = kc != SENTINEL
+    assert np.array_equal(hk[~written], kc[~written])
+    assert ulp_distance(hk[written], kc[written]).max() <= 1
+
+
+def test_inject_refuses_pageable_host_pool():
+    # host memory that is not page-locked has no device mapping: refused on the host,
+    # nothing launched, the cache untouched
+    D, dt = 128, W.BF16
+    cs = _inject_case(D, dt, seed=12)
+    L, Hkv, B, NB, c = cs["L"], cs["Hkv"], cs["B"], cs["NB"], cs["c"]
+    host = np.ascontiguousarray(cs["pool"])
+    assert host.ctypes.data % 16 == 0
+
+    class PageablePool:  # the descriptor as a C caller would fill it
+        def __init__(self):
+            self._s = K._Pool(L, Hkv, D, c, host.shape[0], dt, host.ctypes.data)
+
+        @property
+        def ref(self):
+            return ctypes.byref(self._s)
+
+    cache = K.Cache(torch.zeros((L, NB, Hkv, B, D), dtype=torch.bfloat16, device="cuda"),
+                    torch.zeros((L, NB, Hkv, B, D), dtype=torch.bfloat16, device="cuda"))
+    rope = K.make_rope(1e4, D, 200)
+    with pytest.raises(K.KvinjError) as e:
+        K.kvinj_inject(PageablePool(), cache, rope, i32(cs["ids"]), i32(cs["start"]),
+                       torch.from_numpy(cs["slots"]).cuda())
+    assert e.value.code == K.KVINJ_EINVAL
+    torch.cuda.synchronize()
+    assert not cache.k.any() and not cache.v.any()
 
 
 def test_inject_empty_is_noop():
