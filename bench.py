@@ -411,6 +411,15 @@ def run_gpu(args):
     dec_gbs = per_launch_decode / (dec_avg * 1e-3) / 1e9
     inj_gbs = nbytes["inject"] / (inj_avg * 1e-3) / 1e9
     inj_tok_s = wl.n_inj * cfg.chunk_len / (inj_avg * 1e-3)
+    # copy-on-write block copies: one call over distinct blocks in use, each copied onto
+    # itself (the cache keeps its contents; every record is read and written in full)
+    n_copy = min(1024, cfg.batch * max(1, int(wl.context_lens.min()) // cfg.block_size))
+    copy_ids = inp.block_tables[:, : max(1, n_copy // cfg.batch)].reshape(-1)[:n_copy].contiguous()
+    n_copy = copy_ids.numel()
+    rec_bytes = cfg.kv_heads * cfg.block_size * cfg.head_dim * 2
+    copy_bytes = 2 * 2 * n_copy * cfg.layers * rec_bytes  # K and V, read and write
+    copy_avg = part_ms(lambda: eng.copy_blocks(copy_ids, copy_ids), max(3, args.steps))
+    copy_gbs = copy_bytes / (copy_avg * 1e-3) / 1e9
     peak, peak_kind = _peaks()
     # slot mapping, inject (one launch, or one per layer when overlapped), then per step and
     # layer the append + decode launches
@@ -482,6 +491,10 @@ def run_gpu(args):
                        "pct_of_8tbs": 100 * dec_gbs / NOMINAL_HBM_GBS,
                        "tokens_per_s": ws * cfg.batch * cfg.steps / (ms_step * 1e-3),
                        "bytes_per_launch": per_launch_decode},
+            "copy_blocks": {"blocks": n_copy, "layers": cfg.layers, "bytes": copy_bytes,
+                            "ms": copy_avg, "gbs": copy_gbs,
+                            "note": "each block copied onto itself: full reads and writes, "
+                                    "cache unchanged"},
             "step_bytes": nbytes,
         },
         "roofline": {"kernel": "decode", "bound": "hbm", "achieved": dec_gbs, "peak": peak,
@@ -495,6 +508,9 @@ def run_gpu(args):
                             {"kernel": "inject", "bound": "hbm", "achieved": inj_gbs,
                              "peak": peak, "unit": "GB/s", "frac": inj_gbs / peak,
                              "traffic": _traffic_from_profile(f"inject_{cfg.name}")}),
+        "roofline_copy_blocks": {"kernel": "copy_blocks", "bound": "hbm", "achieved": copy_gbs,
+                                 "peak": peak, "unit": "GB/s", "frac": copy_gbs / peak,
+                                 "traffic": _traffic_from_profile(f"copy_blocks_{cfg.name}")},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,

@@ -153,6 +153,22 @@ int kvinj_inject(const kvinj_pool *pool, const kvinj_cache *cache, const kvinj_r
                  const int64_t *slot_mapping, int32_t n_inj, int32_t layer_begin,
                  int32_t layer_end, int32_t *dev_status, kvinj_stream_t stream);
 
+/* Copy-on-write of shared blocks ("LLM Inference: KV Caching", Paged attention:
+ * two sequences may point at one physical block, which is duplicated only when
+ * one of them writes; "Inside LLM Inference Engines", PagedAttention: prefix
+ * blocks shared read-only with copy-on-write; "Latency Optimization > KV Cache
+ * Management": beams share the prompt's pages, diverging pages are copied).
+ * For i < n and each layer l in [layer_begin, layer_end): block src[i] of layer
+ * l is copied to block dst[i] of layer l, in k and in v (Hkv*B*D elements each,
+ * bit for bit). src, dst: device int32 [n] physical block ids; the caller then
+ * points the writer's block-table entry at dst[i]. A pair with an id outside
+ * [0, num_blocks) is skipped and sets KVINJ_ST_BAD_BLOCK. Pairs whose dst is
+ * another pair's src or dst race (undefined which copy wins). n == 0 or an
+ * empty layer range is a no-op. */
+int kvinj_copy_blocks(const kvinj_cache *cache, const int32_t *src, const int32_t *dst, int64_t n,
+                      int32_t layer_begin, int32_t layer_end, int32_t *dev_status,
+                      kvinj_stream_t stream);
+
 /* Append ("LLM Inference: KV Caching", The fix): token i < n writes
  * k_new[i][h][:] rotated at positions[i] (copied as given when rope == NULL)
  * and v_new[i][h][:] to layer `layer` at slot_mapping[i].

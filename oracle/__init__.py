@@ -1,7 +1,7 @@
 """fp64 CPU oracle for the paged KV-injection path -- TEST INFRASTRUCTURE.
 
 A plain, slow statement of what the path computes (RoPE, slot mapping,
-inject, append, paged decode attention), written in C in ``kvinj_oracle.c``
+inject, append, block copies, paged decode attention), written in C in ``kvinj_oracle.c``
 and wrapped here with ctypes over numpy arrays. It shares no code with the
 CUDA library in ``paged_kv_cache_inject_gb300``, and neither imports the
 other. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg
@@ -69,6 +69,8 @@ def _load():
                 "orc_append": (i32, [P, P, ctypes.c_int, ctypes.c_int, i64, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_int, P, P, P, P, i64, ctypes.c_int,
                                      f64]),
+                "orc_copy_blocks": (i32, [P, P, ctypes.c_int, ctypes.c_int, i64, ctypes.c_int,
+                                          P, P, i64, ctypes.c_int, ctypes.c_int]),
                 "orc_attention": (f64, [P, P, P, i64, ctypes.c_int, f64, P]),
                 "orc_attention_bits": (None, [P, ctypes.c_int, f64, f64, P, P, i64, ctypes.c_int,
                                               ctypes.c_int, f64, P]),
@@ -201,6 +203,16 @@ def append(k_cache, v_cache, layer, k_new, v_new, positions, slot_map, theta, dt
     return int(_load().orc_append(_p(k_cache), _p(v_cache), Hkv, D, NB, B, dtype, layer,
                                   _p(kn), _p(vn), _p(pos), _p(sm), pos.size, int(rotate),
                                   float(theta)))
+
+
+def copy_blocks(k_cache, v_cache, src, dst, layer_begin=0, layer_end=None) -> int:
+    """In place: block src[i] -> dst[i] in layers [layer_begin, layer_end), K and V."""
+    L, NB, Hkv, B, D = k_cache.shape
+    s = _c(src, np.int32)
+    d = _c(dst, np.int32)
+    le = L if layer_end is None else layer_end
+    return int(_load().orc_copy_blocks(_p(k_cache), _p(v_cache), Hkv, D, NB, B, _p(s), _p(d),
+                                       s.size, layer_begin, le))
 
 
 # ---- attention ------------------------------------------------------------

@@ -252,6 +252,37 @@ int32_t orc_append(uint16_t *k_cache, uint16_t *v_cache, int Hkv, int D, int64_t
 }
 
 /* ------------------------------------------------------------------ */
+/* Copy-on-write of a shared block [KC "Paged attention": a block two   */
+/* sequences point at is duplicated when one of them writes; IE          */
+/* "PagedAttention" item 4; KM (beams copy only diverging pages)]. For   */
+/* each pair i and layer l in [l0, l1): every element of block src[i]    */
+/* of layer l, K and V, is copied to block dst[i]. Pairs with an id      */
+/* outside the cache are skipped (status bit).                           */
+/* ------------------------------------------------------------------ */
+int32_t orc_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, int Hkv, int D, int64_t num_blocks,
+                        int B, const int32_t *src, const int32_t *dst, int64_t n, int l0,
+                        int l1) {
+  int32_t st = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    if (src[i] < 0 || src[i] >= num_blocks || dst[i] < 0 || dst[i] >= num_blocks) {
+      st |= ORC_ST_BLOCK;
+      continue;
+    }
+    for (int l = l0; l < l1; ++l)
+      for (int h = 0; h < Hkv; ++h)
+        for (int t = 0; t < B; ++t) {
+          int64_t from = cache_row(l, (int64_t)src[i] * B + t, h, num_blocks, Hkv, B, D);
+          int64_t to = cache_row(l, (int64_t)dst[i] * B + t, h, num_blocks, Hkv, B, D);
+          for (int d = 0; d < D; ++d) {
+            k_cache[to + d] = k_cache[from + d];
+            v_cache[to + d] = v_cache[from + d];
+          }
+        }
+  }
+  return st;
+}
+
+/* ------------------------------------------------------------------ */
 /* Textbook attention for one query over a contiguous key/value list    */
 /* [KC "First, what K and V are"]: s_j = scale * q.K_j, w = softmax(s)  */
 /* (max-subtracted), out = sum_j w_j V_j. Also returns sum_j w_j.        */

@@ -204,6 +204,29 @@ int kvinj_inject(const kvinj_pool *pool, const kvinj_cache *cache, const kvinj_r
   return cuda_rc(launch_inject(a, cache->head_dim, cache->dtype, (cudaStream_t)stream));
 }
 
+int kvinj_copy_blocks(const kvinj_cache *cache, const int32_t *src, const int32_t *dst, int64_t n,
+                      int32_t layer_begin, int32_t layer_end, int32_t *dev_status,
+                      kvinj_stream_t stream) {
+  int rc = check_cache(cache, false);
+  if (rc) return rc;
+  if (n < 0 || layer_begin < 0 || layer_end > cache->num_layers || layer_begin > layer_end)
+    return KVINJ_EINVAL;
+  if (n == 0 || layer_begin == layer_end) return KVINJ_OK;
+  if (!src || !dst) return KVINJ_EINVAL;
+  CopyBlocksArgs a;
+  a.k = static_cast<uint8_t *>(cache->k);
+  a.v = static_cast<uint8_t *>(cache->v);
+  a.num_blocks = cache->num_blocks;
+  a.rec_bytes = (int64_t)cache->num_kv_heads * cache->block_size * cache->head_dim * 2;
+  a.src = src;
+  a.dst = dst;
+  a.n = n;
+  a.layer_begin = layer_begin;
+  a.n_layers = layer_end - layer_begin;
+  a.status = dev_status;
+  return cuda_rc(launch_copy_blocks(a, (cudaStream_t)stream));
+}
+
 int kvinj_append(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
                  const void *k_new, const void *v_new, const int32_t *positions,
                  const int64_t *slot_mapping, int64_t n, int32_t *dev_status,

@@ -272,4 +272,60 @@ cudaError_t launch_append(const AppendArgs &a, int D, int dtype, cudaStream_t s)
   return cudaErrorInvalidValue;
 }
 
+// ---------------------------------------------------------------------------
+// block copy (copy-on-write of a shared block)
+// ---------------------------------------------------------------------------
+// "LLM Inference: KV Caching", Paged attention: once blocks are first-class, two
+// sequences can point at the same one and a block is duplicated only when one of them
+// writes; "Inside LLM Inference Engines", PagedAttention item 4 (prefix blocks shared
+// read-only, copy-on-write); "Latency Optimization > KV Cache Management" (beams share
+// the prompt's pages, only diverging pages are copied). A record is one block of one
+// layer of K or V: Hkv*B*D contiguous elements. A CTA copies one record at a time with
+// 16-byte vectors, every load of its share issued before the stores (8 vectors per
+// thread in flight); the grid is persistent and walks (pair, layer, K|V) records.
+constexpr int COPY_THREADS = 256, COPY_VEC = 8;
+
+__global__ void __launch_bounds__(COPY_THREADS) copy_blocks_kernel(CopyBlocksArgs a) {
+  const int64_t nrec = a.n * a.n_layers * 2;
+  const int64_t nvec = a.rec_bytes / 16;
+  int bad = 0;
+  for (int64_t r = blockIdx.x; r < nrec; r += gridDim.x) {
+    const int kv = (int)(r & 1);
+    const int64_t pl = r >> 1;
+    const int l = a.layer_begin + (int)(pl % a.n_layers);
+    const int64_t i = pl / a.n_layers;
+    const int64_t sb = a.src[i], db = a.dst[i];
+    if (sb < 0 || sb >= a.num_blocks || db < 0 || db >= a.num_blocks) {
+      bad = KVINJ_ST_BAD_BLOCK;
+      continue;
+    }
+    uint8_t *base = kv ? a.v : a.k;
+    const uint4 *src = reinterpret_cast<const uint4 *>(base + ((int64_t)l * a.num_blocks + sb) *
+                                                                  a.rec_bytes);
+    uint4 *dst = reinterpret_cast<uint4 *>(base + ((int64_t)l * a.num_blocks + db) * a.rec_bytes);
+    for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += (int64_t)COPY_THREADS * COPY_VEC) {
+      uint4 w[COPY_VEC];
+#pragma unroll
+      for (int k = 0; k < COPY_VEC; ++k) {
+        const int64_t v = v0 + (int64_t)k * COPY_THREADS;
+        if (v < nvec) w[k] = ld_stream(src + v);
+      }
+#pragma unroll
+      for (int k = 0; k < COPY_VEC; ++k) {
+        const int64_t v = v0 + (int64_t)k * COPY_THREADS;
+        if (v < nvec) st_global(dst + v, w[k]);
+      }
+    }
+  }
+  if (bad && threadIdx.x == 0) report(a.status, bad);
+}
+
+cudaError_t launch_copy_blocks(const CopyBlocksArgs &a, cudaStream_t s) {
+  const int64_t nrec = a.n * a.n_layers * 2;
+  int64_t ctas = (int64_t)num_sms() * 8;
+  if (ctas > nrec) ctas = nrec;
+  copy_blocks_kernel<<<(int)(ctas < 1 ? 1 : ctas), COPY_THREADS, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace kvinj

@@ -71,6 +71,18 @@ cudaError_t launch_slot_mapping(const int32_t *bt, int max_blocks, int batch, in
                                 int64_t *out, int32_t *status, cudaStream_t s);
 cudaError_t launch_inject(const InjectArgs &a, int D, int dtype, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs &a, int D, int dtype, cudaStream_t s);
+
+// block copies for copy-on-write: record (pair i, layer, K|V) of rec_bytes bytes each
+struct CopyBlocksArgs {
+  uint8_t *k, *v;            // cache base pointers
+  int64_t num_blocks;        // physical blocks per layer
+  int64_t rec_bytes;         // bytes of one block of one layer: Hkv * B * D * 2
+  const int32_t *src, *dst;  // [n] physical block ids
+  int64_t n;
+  int layer_begin, n_layers;
+  int32_t *status;
+};
+cudaError_t launch_copy_blocks(const CopyBlocksArgs &a, cudaStream_t s);
 // HG: kv heads per work unit (a power of two <= 8 dividing Hkv)
 int decode_head_group(int Hkv);
 cudaError_t launch_decode_ffma(const DecodeArgs &a, const CUtensorMap &tmK,

@@ -94,6 +94,11 @@ class Engine:
                                     0.0, self.status, None, self.decode_variant,
                                     self.decode_ctas)
 
+    def copy_blocks(self, src: torch.Tensor, dst: torch.Tensor, layer_begin: int = 0,
+                    layer_end: int | None = None):
+        """Copy-on-write: physical block src[i] -> dst[i] in every layer (K and V)."""
+        K.kvinj_copy_blocks(self.cache, src, dst, layer_begin, layer_end, self.status)
+
     def uses_tcgen05(self) -> bool:
         """Whether decode runs the tcgen05 kernel (one launch per layer)."""
         G = self.Hq // self.Hkv

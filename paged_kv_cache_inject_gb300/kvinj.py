@@ -29,7 +29,7 @@ EXPORTS = [
     "kvinj_append", "kvinj_decode_workspace_size", "kvinj_decode_workspace_init",
     "kvinj_paged_decode", "kvinj_paged_decode_ex", "kvinj_append_paged_decode",
     "kvinj_append_paged_decode_ex", "kvinj_paged_decode_static", "kvinj_kv_bytes",
-    "kvinj_strerror",
+    "kvinj_strerror", "kvinj_copy_blocks",
 ]
 
 
@@ -79,6 +79,7 @@ def load(path: str = LIB_PATH):
             "kvinj_slot_mapping": (ctypes.c_int, [P, i32, i32, i64, i32, P, P, i64, P, P, P]),
             "kvinj_inject": (ctypes.c_int, [P, P, P, P, P, P, i32, i32, i32, P, P]),
             "kvinj_append": (ctypes.c_int, [P, P, i32, P, P, P, P, i64, P, P]),
+            "kvinj_copy_blocks": (ctypes.c_int, [P, P, P, i64, i32, i32, P, P]),
             "kvinj_decode_workspace_size": (sz, [i32, i32, i32, i32]),
             "kvinj_decode_workspace_init": (ctypes.c_int, [P, sz, P]),
             "kvinj_paged_decode": (ctypes.c_int, [P, P, i32, i32, P, P, P, i32, P, i32,
@@ -226,6 +227,17 @@ def kvinj_inject(pool: Pool, cache: Cache, rope: Rope, chunk_ids, start_pos, slo
            load().kvinj_inject(pool.ref, cache.ref, rope.ref, _ptr(chunk_ids), _ptr(start_pos),
                                _ptr(slot_mapping), chunk_ids.numel(), layer_begin, le,
                                _ptr(status), _stream(stream)))
+
+
+def kvinj_copy_blocks(cache: Cache, src, dst, layer_begin: int = 0, layer_end: int | None = None,
+                      status=None, stream=None):
+    """Copy physical block src[i] to dst[i] in every layer of [layer_begin, layer_end), K and
+    V (int32 device tensors of equal length): the copy-on-write of a shared block."""
+    assert src.dtype == torch.int32 and dst.dtype == torch.int32 and src.numel() == dst.numel()
+    le = cache.num_layers if layer_end is None else layer_end
+    _check("kvinj_copy_blocks",
+           load().kvinj_copy_blocks(cache.ref, _ptr(src), _ptr(dst), src.numel(), layer_begin, le,
+                                    _ptr(status), _stream(stream)))
 
 
 def kvinj_append(cache: Cache, rope: Rope | None, layer: int, k_new, v_new, positions,

@@ -226,6 +226,84 @@ def test_inject_refuses_pageable_host_pool():
     assert not cache.k.any() and not cache.v.any()
 
 
+@pytest.mark.parametrize("D,dt", [(128, W.BF16), (64, W.FP16), (256, W.BF16)])
+def test_copy_blocks_matches_oracle(D, dt):
+    # copy-on-write block copies: bit-exact, only the listed layers, bad ids skipped
+    rng = np.random.default_rng(31 + D)
+    L, NB, Hkv, B = 3, 40, 4, 16
+    tdt = torch_dtype(dt)
+    kc = gen_bits(31, (L, NB, Hkv, B, D), dt)
+    vc = gen_bits(32, (L, NB, Hkv, B, D), dt)
+    perm = rng.permutation(NB).astype(np.int32)
+    src, dst = perm[:13].copy(), perm[13:26].copy()
+    src[4] = NB + 3  # an id outside the cache: skipped, flagged
+    want_k, want_v = kc.copy(), vc.copy()
+    assert oracle.copy_blocks(want_k, want_v, src, dst, 1, 3) == 4
+    cache = K.Cache(from_bits(kc, tdt), from_bits(vc, tdt))
+    status = status_tensor()
+    K.kvinj_copy_blocks(cache, i32(src), i32(dst), 1, 3, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == K.ST_BAD_BLOCK
+    assert np.array_equal(bits(cache.k), want_k) and np.array_equal(bits(cache.v), want_v)
+    # empty calls change nothing
+    K.kvinj_copy_blocks(cache, i32(src[:0]), i32(dst[:0]))
+    K.kvinj_copy_blocks(cache, i32(src), i32(dst), 2, 2)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(cache.k), want_k)
+
+
+def test_copy_on_write_then_append_and_decode():
+    # two requests share a prefix of blocks; the second writes into the shared, partly
+    # filled last block: it gets a private copy first, then appends its token and both
+    # decode (the reader's output bit for bit as before the write)
+    D, G, dt, Hkv, theta = 128, 4, W.BF16, 8, 5e5
+    tdt = torch_dtype(dt)
+    ctx = 1000  # 63 pages, the last holding 8 tokens
+    kc, vc, q, bt = _decode_case(D, G, dt, [ctx], Hkv=Hkv, L=2, seed=33, spare=4)
+    NB = kc.shape[1]
+    free = int(np.setdiff1d(np.arange(NB), bt[0][bt[0] >= 0])[0])
+    pages = -(-ctx // 16)
+    bt_a = bt.copy()
+    bt_b = bt.copy()
+    bt_b[0, pages - 1] = free
+    qb = gen_bits(34, q.shape, dt)
+    kn = gen_bits(35, (1, Hkv, D), dt)
+    vn = gen_bits(36, (1, Hkv, D), dt)
+    slot = np.array([free * 16 + ctx % 16], np.int64)
+    # oracle
+    ek, ev = kc.copy(), vc.copy()
+    assert oracle.copy_blocks(ek, ev, [bt[0, pages - 1]], [free]) == 0
+    assert oracle.append(ek, ev, 1, kn, vn, [ctx], slot, theta, dt) == 0
+    want_a, _ = oracle.paged_decode(ek, ev, 1, q, [ctx - 1], bt_a, [ctx], theta, dt)
+    want_b, _ = oracle.paged_decode(ek, ev, 1, qb, [ctx], bt_b, [ctx + 1], theta, dt)
+    # library
+    cache = K.Cache(from_bits(kc, tdt), from_bits(vc, tdt))
+    rope = K.make_rope(theta, D, ctx + 8)
+    ws = K.make_decode_workspace(1, Hkv * G, Hkv, D)
+    status = status_tensor()
+
+    def decode(qbits, pos, table, c):
+        out = torch.empty((1, Hkv * G, D), dtype=tdt, device="cuda")
+        K.kvinj_paged_decode(cache, rope, 1, from_bits(qbits, tdt), i32(np.array([pos])),
+                             i32(table), i32(np.array([c])), out, ws, 0.0, status)
+        torch.cuda.synchronize()
+        return out.float().cpu().numpy().astype(np.float64)
+
+    before_a = decode(q, ctx - 1, bt_a, ctx)
+    K.kvinj_copy_blocks(cache, i32(np.array([bt[0, pages - 1]])), i32(np.array([free])),
+                        status=status)
+    K.kvinj_append(cache, rope, 1, from_bits(kn, tdt), from_bits(vn, tdt),
+                   i32(np.array([ctx])), torch.from_numpy(slot).cuda(), status=status)
+    got_a = decode(q, ctx - 1, bt_a, ctx)
+    got_b = decode(qb, ctx, bt_b, ctx + 1)
+    assert status.item() == 0
+    assert np.array_equal(got_a, before_a)
+    assert_decode_close(got_a, want_a, "reader after copy-on-write")
+    assert_decode_close(got_b, want_b, "writer after copy-on-write")
+    assert ulp_distance(bits(cache.k), ek).max() <= 1  # the appended K is rotated
+    assert np.array_equal(bits(cache.v), ev)
+
+
 def test_inject_empty_is_noop():
     D = 64
     cache = K.Cache(torch.zeros((1, 2, 1, 16, D), dtype=torch.bfloat16, device="cuda"),

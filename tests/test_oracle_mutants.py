@@ -39,6 +39,9 @@ MUTANTS = [
      "int32_t blk = block_tables[(int64_t)r * max_blocks + j % B];"),
     ("decode_query_not_rotated", "if (rotate_q) orc_rope(q0, D, q_pos, theta, q);",
      "if (0) orc_rope(q0, D, q_pos, theta, q);"),
+    ("copy_blocks_first_layer_only", "for (int l = l0; l < l1; ++l)\n      for (int h = 0; h < Hkv; ++h)\n        for (int t = 0; t < B; ++t) {",
+     "for (int l = l0; l < l0 + 1; ++l)\n      for (int h = 0; h < Hkv; ++h)\n        for (int t = 0; t < B; ++t) {"),
+    ("copy_blocks_k_only", "            v_cache[to + d] = v_cache[from + d];\n", ""),
 ]
 
 

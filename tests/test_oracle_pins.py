@@ -327,6 +327,63 @@ def test_paged_equals_contiguous_under_block_permutations():
         assert np.array_equal(results[0][0, qh], want)
 
 
+def test_copy_on_write_shared_prefix():
+    # Two sequences point at the same physical blocks; one of them writes into the shared,
+    # partly filled last block, which is therefore duplicated first and the writer's table
+    # pointed at the copy ("LLM Inference: KV Caching", Paged attention; "Inside LLM
+    # Inference Engines", PagedAttention, copy-on-write). Afterwards the reader's attention
+    # is unchanged, and the writer's equals textbook attention over its own logical token
+    # list (the shared prefix, then its new token), computed from contiguous arrays.
+    rng = np.random.default_rng(21)
+    L, B, NB, Hkv, G, D, theta = 2, 16, 8, 2, 2, 64, 5e5
+    Hq = Hkv * G
+    ctx = 37  # three pages, the last one holds 5 tokens
+    Kc = oracle.encode(rng.standard_normal((ctx, Hkv, D)), BF16)
+    Vc = oracle.encode(rng.standard_normal((ctx, Hkv, D)), BF16)
+    shared = np.array([5, 2, 6], np.int32)
+    kc = oracle.encode(rng.standard_normal((L, NB, Hkv, B, D)), BF16)  # anything elsewhere
+    vc = oracle.encode(rng.standard_normal((L, NB, Hkv, B, D)), BF16)
+    for p in range(ctx):
+        kc[1, shared[p // B], :, p % B] = Kc[p]
+        vc[1, shared[p // B], :, p % B] = Vc[p]
+    qa = oracle.encode(rng.standard_normal((1, Hq, D)), BF16)
+    qb = oracle.encode(rng.standard_normal((1, Hq, D)), BF16)
+    bt_a = shared[None]
+    out_a, st = oracle.paged_decode(kc, vc, 1, qa, [ctx - 1], bt_a, [ctx], theta, BF16)
+    assert st == 0
+    k0, v0 = kc.copy(), vc.copy()
+    # the writer's copy of the last shared block, then its new token at position ctx
+    free = 3
+    assert oracle.copy_blocks(kc, vc, [shared[-1]], [free]) == 0
+    bt_b = np.array([[shared[0], shared[1], free]], np.int32)
+    kn = oracle.encode(rng.standard_normal((1, Hkv, D)), BF16)
+    vn = oracle.encode(rng.standard_normal((1, Hkv, D)), BF16)
+    assert oracle.append(kc, vc, 1, kn, vn, [ctx], [free * B + ctx % B], theta, BF16) == 0
+    # the reader sees exactly what it saw before
+    again, _ = oracle.paged_decode(kc, vc, 1, qa, [ctx - 1], bt_a, [ctx], theta, BF16)
+    assert np.array_equal(again, out_a)
+    # the writer sees the shared prefix and its own token
+    out_b, st = oracle.paged_decode(kc, vc, 1, qb, [ctx], bt_b, [ctx + 1], theta, BF16)
+    assert st == 0
+    for qh in range(Hq):
+        h = qh // G
+        k_new = oracle.rope_round_rows(kn[0, h][None], [ctx], theta, BF16)
+        K = np.concatenate([Kc[:, h], k_new])
+        V = np.concatenate([Vc[:, h], vn[0, h][None]])
+        want = oracle.attention_bits(qb[0, qh], ctx, theta, K, V, BF16)
+        assert np.array_equal(out_b[0, qh], want)
+    # every layer was copied; no block other than the copy changed
+    for l in range(L):
+        assert np.array_equal(kc[l, free, :, : ctx % B], k0[l, shared[-1], :, : ctx % B])
+        assert np.array_equal(vc[0, free], v0[0, shared[-1]])
+    others = [b for b in range(NB) if b != free]
+    assert np.array_equal(kc[:, others], k0[:, others]) and np.array_equal(vc[:, others], v0[:, others])
+    # ids outside the cache are flagged and skipped
+    k1, v1 = kc.copy(), vc.copy()
+    assert oracle.copy_blocks(kc, vc, [0, NB], [1, 2]) == 4
+    assert np.array_equal(kc[:, 1], k1[:, 0]) and np.array_equal(kc[:, 2], k1[:, 2])
+
+
 def test_gqa_groups_are_consecutive_query_heads():
     # "groups of four share one key and value head" ("LLM Inference: KV Caching");
     # reading: query heads g*G .. g*G+G-1 use kv head g
