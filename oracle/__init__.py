@@ -77,7 +77,7 @@ def _load():
                 "orc_paged_decode": (i32, [P, P, ctypes.c_int, ctypes.c_int, i64, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
                                            ctypes.c_int, f64, P, ctypes.c_int, P, ctypes.c_int,
-                                           f64, P, ctypes.c_int]),
+                                           f64, P, ctypes.c_int, ctypes.c_int]),
                 "orc_has_openmp": (ctypes.c_int, []),
             }
             for name, (res, args) in sig.items():
@@ -239,8 +239,9 @@ def attention_bits(q_bits, q_pos, theta, K_bits, V_bits, dtype, scale=0.0, rotat
 
 
 def paged_decode(k_cache, v_cache, layer, q_bits, q_pos, block_tables, context_lens, theta,
-                 dtype, scale=0.0, rotate_q=True, n_threads=1):
-    """q_bits[batch][Hq][D]; returns (out fp64 [batch][Hq][D], status)."""
+                 dtype, scale=0.0, rotate_q=True, n_threads=1, window=0):
+    """q_bits[batch][Hq][D]; returns (out fp64 [batch][Hq][D], status). window > 0: each
+    query attends to the last `window` tokens of its context only."""
     L, NB, Hkv, B, D = k_cache.shape
     q = _c(q_bits, np.uint16)
     batch, Hq, _ = q.shape
@@ -250,5 +251,6 @@ def paged_decode(k_cache, v_cache, layer, q_bits, q_pos, block_tables, context_l
     out = np.empty((batch, Hq, D), np.float64)
     st = _load().orc_paged_decode(_p(k_cache), _p(v_cache), Hkv, D, NB, B, dtype, layer, Hq,
                                   _p(q), _p(qp), int(rotate_q), float(theta), _p(bt),
-                                  bt.shape[1], _p(cl), batch, float(scale), _p(out), n_threads)
+                                  bt.shape[1], _p(cl), batch, float(scale), _p(out), n_threads,
+                                  int(window))
     return out, int(st)

@@ -344,7 +344,7 @@ int32_t orc_paged_decode(const uint16_t *k_cache, const uint16_t *v_cache, int H
                          const uint16_t *q, const int32_t *q_pos, int rotate_q, double theta,
                          const int32_t *block_tables, int max_blocks,
                          const int32_t *context_lens, int batch, double scale, double *out,
-                         int n_threads) {
+                         int n_threads, int window) {
   int32_t st = 0;
   int G = Hq / Hkv;
   if (scale <= 0.0) scale = 1.0 / sqrt((double)D);
@@ -355,19 +355,22 @@ int32_t orc_paged_decode(const uint16_t *k_cache, const uint16_t *v_cache, int H
     for (int d = 0; d < D; ++d) o[d] = 0.0;
     int64_t ctx = context_lens[r];
     if (ctx <= 0 || ctx > (int64_t)max_blocks * B) { st |= ORC_ST_CTX; continue; }
-    uint16_t *Kr = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)ctx * D);
-    uint16_t *Vr = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)ctx * D);
+    /* sliding window [KC "sliding window attention"]: only the last `window` tokens of the */
+    /* context are attended to (window <= 0: all of them); only their blocks are read      */
+    int64_t j0 = (window > 0 && ctx > window) ? ctx - window : 0, n = ctx - j0;
+    uint16_t *Kr = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)n * D);
+    uint16_t *Vr = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)n * D);
     int bad = 0;
-    for (int64_t j = 0; j < ctx; ++j) {
+    for (int64_t j = j0; j < ctx; ++j) {
       int32_t blk = block_tables[(int64_t)r * max_blocks + j / B];
       if (blk < 0 || blk >= num_blocks) { bad = 1; break; }
       int64_t src = cache_row(layer, (int64_t)blk * B + j % B, h, num_blocks, Hkv, B, D);
-      memcpy(Kr + j * D, k_cache + src, sizeof(uint16_t) * D);
-      memcpy(Vr + j * D, v_cache + src, sizeof(uint16_t) * D);
+      memcpy(Kr + (j - j0) * D, k_cache + src, sizeof(uint16_t) * D);
+      memcpy(Vr + (j - j0) * D, v_cache + src, sizeof(uint16_t) * D);
     }
     if (bad) st |= ORC_ST_BLOCK;
     else
-      orc_attention_bits(q + rq * D, rotate_q, (double)q_pos[r], theta, Kr, Vr, ctx, D, dtype,
+      orc_attention_bits(q + rq * D, rotate_q, (double)q_pos[r], theta, Kr, Vr, n, D, dtype,
                          scale, o);
     free(Kr);
     free(Vr);

@@ -41,6 +41,8 @@ MUTANTS = [
      "if (0) orc_rope(q0, D, q_pos, theta, q);"),
     ("copy_blocks_first_layer_only", "for (int l = l0; l < l1; ++l)\n      for (int h = 0; h < Hkv; ++h)\n        for (int t = 0; t < B; ++t) {",
      "for (int l = l0; l < l0 + 1; ++l)\n      for (int h = 0; h < Hkv; ++h)\n        for (int t = 0; t < B; ++t) {"),
+    ("window_off_by_one", "int64_t j0 = (window > 0 && ctx > window) ? ctx - window : 0",
+     "int64_t j0 = (window > 0 && ctx > window) ? ctx - window + 1 : 0"),
     ("copy_blocks_k_only", "            v_cache[to + d] = v_cache[from + d];\n", ""),
 ]
 

@@ -384,6 +384,41 @@ def test_copy_on_write_shared_prefix():
     assert np.array_equal(kc[:, 1], k1[:, 0]) and np.array_equal(kc[:, 2], k1[:, 2])
 
 
+def test_sliding_window_decode():
+    # under a sliding window a query attends only to the last W tokens ("LLM Inference: KV
+    # Caching", sliding window attention): equal to textbook attention over the contiguous
+    # last W tokens; W >= ctx is full attention; blocks wholly before the window are not read
+    rng = np.random.default_rng(23)
+    B, NB, Hkv, G, D, theta = 16, 12, 2, 2, 64, 5e5
+    Hq = Hkv * G
+    ctx = 150
+    Kc = oracle.encode(rng.standard_normal((ctx, Hkv, D)), BF16)
+    Vc = oracle.encode(rng.standard_normal((ctx, Hkv, D)), BF16)
+    q = oracle.encode(rng.standard_normal((1, Hq, D)), BF16)
+    perm = rng.permutation(NB)[:10].astype(np.int32)
+    kc, vc = _scatter_to_paged(Kc, Vc, perm, B, NB, Hkv, D, BF16)
+    bt = perm.reshape(1, -1)
+    full, st = oracle.paged_decode(kc, vc, 0, q, [ctx - 1], bt, [ctx], theta, BF16)
+    assert st == 0
+    for W in (ctx, ctx + 7):
+        out, st = oracle.paged_decode(kc, vc, 0, q, [ctx - 1], bt, [ctx], theta, BF16, window=W)
+        assert st == 0 and np.array_equal(out, full)
+    for W in (1, 16, 37, 149):
+        out, st = oracle.paged_decode(kc, vc, 0, q, [ctx - 1], bt, [ctx], theta, BF16, window=W)
+        assert st == 0
+        for qh in range(Hq):
+            h = qh // G
+            want = oracle.attention_bits(q[0, qh], ctx - 1, theta, Kc[ctx - W:, h], Vc[ctx - W:, h],
+                                         BF16)
+            assert np.array_equal(out[0, qh], want)
+    # table entries of pages wholly before the window may be anything
+    bt2 = bt.copy()
+    bt2[0, :5] = -1
+    out, st = oracle.paged_decode(kc, vc, 0, q, [ctx - 1], bt2, [ctx], theta, BF16, window=60)
+    want, _ = oracle.paged_decode(kc, vc, 0, q, [ctx - 1], bt, [ctx], theta, BF16, window=60)
+    assert st == 0 and np.array_equal(out, want)
+
+
 def test_gqa_groups_are_consecutive_query_heads():
     # "groups of four share one key and value head" ("LLM Inference: KV Caching");
     # reading: query heads g*G .. g*G+G-1 use kv head g
