@@ -62,13 +62,16 @@ def _dist():
 # replicas: nothing on the path exchanges data between GPUs; each rank runs
 # its own batch and only the timing is reduced
 # ---------------------------------------------------------------------------
-def workload_config(cfg) -> dict:
+def workload_config(cfg, window: int = 0) -> dict:
     """The workload's identity in the JSON line (shared by both arms)."""
-    return {"workload": cfg.name, "layers": cfg.layers, "q_heads": cfg.q_heads,
-            "kv_heads": cfg.kv_heads, "head_dim": cfg.head_dim, "block_size": cfg.block_size,
-            "batch": cfg.batch, "context": list(cfg.ctx),
-            "injected_chunks_per_request": cfg.chunks_per_req, "chunk_len": cfg.chunk_len,
-            "pool_chunks": cfg.pool_chunks, "decode_steps": cfg.steps}
+    c = {"workload": cfg.name, "layers": cfg.layers, "q_heads": cfg.q_heads,
+         "kv_heads": cfg.kv_heads, "head_dim": cfg.head_dim, "block_size": cfg.block_size,
+         "batch": cfg.batch, "context": list(cfg.ctx),
+         "injected_chunks_per_request": cfg.chunks_per_req, "chunk_len": cfg.chunk_len,
+         "pool_chunks": cfg.pool_chunks, "decode_steps": cfg.steps}
+    if window:
+        c["decode_window"] = window  # sliding window: the last `window` tokens of each context
+    return c
 
 
 def replica_seed(cfg_seed: int, rank: int) -> int:
@@ -182,11 +185,11 @@ class OracleSample:
     append of the context and step tokens, and paged decode of every query
     head of every request. Inputs are generated once (not timed)."""
 
-    def __init__(self, wl, threads: int):
+    def __init__(self, wl, threads: int, window: int = 0):
         import numpy as np
 
         import oracle
-        self.np, self.oracle, self.wl, self.threads = np, oracle, wl, threads
+        self.np, self.oracle, self.wl, self.threads, self.window = np, oracle, wl, threads, window
         cfg = wl.cfg
         L0 = 0
         Hkv, D, c = cfg.kv_heads, cfg.head_dim, cfg.chunk_len
@@ -212,8 +215,10 @@ class OracleSample:
         row = Hkv * D * cfg.elem_bytes
         n_inj_tok = wl.n_inj * c
         n_app = sum(x[0].size for x in self.app)
-        pages = -(-self.ctx.astype(np.int64) // cfg.block_size)
-        self.bytes = (2 * 2 * row * n_inj_tok + 2 * 2 * row * n_app + int(self.ctx.sum()) * 2 * row
+        ctx = self.ctx.astype(np.int64)
+        lo = np.maximum(ctx - window, 0) if window > 0 else np.zeros_like(ctx)
+        pages = -(-ctx // cfg.block_size) - lo // cfg.block_size
+        self.bytes = (2 * 2 * row * n_inj_tok + 2 * 2 * row * n_app + int((ctx - lo).sum()) * 2 * row
                       + cfg.batch * cfg.q_heads * D * 2 * 2 + int(pages.sum()) * 4)
         self.inj_tokens = n_inj_tok
 
@@ -230,7 +235,8 @@ class OracleSample:
             sl, _ = orc.slot_mapping(wl.block_tables, seq, pos, cfg.block_size, wl.num_blocks)
             orc.append(kc, vc, 0, kn, vn, pos, sl, cfg.theta, cfg.dtype)
         out, _ = orc.paged_decode(kc, vc, 0, self.q, self.q_pos, wl.block_tables, self.ctx,
-                                  cfg.theta, cfg.dtype, n_threads=self.threads)
+                                  cfg.theta, cfg.dtype, n_threads=self.threads,
+                                  window=self.window)
         return out
 
     @property
@@ -254,7 +260,7 @@ def run_reference(args):
     import workload as W
     wl = W.make_workload(W.CONFIGS[args.config])
     threads = oracle_threads()
-    sample = OracleSample(wl, threads)
+    sample = OracleSample(wl, threads, args.window)
     for _ in range(args.warmup):
         sample.run()
     t0 = time.perf_counter()
@@ -269,7 +275,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {**workload_config(wl.cfg), "sample": "layer 0 per step (oracle on host cores)"},
+        "config": {**workload_config(wl.cfg, args.window), "sample": "layer 0 per step (oracle on host cores)"},
         "cpu_baseline": cpu,
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "inject_tokens_per_s": sample.inj_tokens / dt,
@@ -315,12 +321,13 @@ def run_gpu(args):
     eng = stage.make_engine(wl, dev, pool=pool)
     eng.decode_variant = args.variant
     eng.overlap_inject = args.overlap_inject
+    eng.window = args.window
     stage.fill_context(eng, wl, dev)
     inp = stage.step_inputs(wl, dev)
     if remap is not None:
         inp.chunk_ids.copy_(torch.from_numpy(remap).to(dev))
     out = eng.alloc_outputs(cfg.steps)
-    nbytes = stage.algorithmic_bytes(wl)
+    nbytes = stage.algorithmic_bytes(wl, args.window)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -452,7 +459,7 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         threads = oracle_threads()
-        sample = OracleSample(wl, threads)
+        sample = OracleSample(wl, threads, args.window)
         # about ten seconds of oracle work: the layer-0 sample, repeated
         runs, t0 = 0, time.perf_counter()
         while True:
@@ -472,7 +479,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": W.DTYPE_NAMES[cfg.dtype],
         "data": "synthetic",
-        "config": {**workload_config(cfg), "parallelism": f"replicas x{ws}",
+        "config": {**workload_config(cfg, args.window), "parallelism": f"replicas x{ws}",
                    "l2": (f"inputs larger than L2: {nbytes['total'] / 1e9:.2f} GB touched per "
                           f"step; no flush"),
                    "decode_variant": args.variant,
@@ -535,6 +542,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly from Python")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling cases only)")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding-window decode over the last W tokens (0: whole context)")
     ap.add_argument("--pool-host", action="store_true",
                     help="keep the chunk pool in pinned host memory (inject reads it in place)")
     ap.add_argument("--compact-pool", action="store_true",

@@ -215,6 +215,24 @@ int kvinj_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t
                        void *workspace, size_t ws_bytes, int32_t *dev_status,
                        kvinj_stream_t stream);
 
+/* Paged decode under a sliding window ("LLM Inference: KV Caching", sliding
+ * window attention: a token attends only to the last W tokens). As
+ * kvinj_paged_decode (with the new token's append fused when k_new and v_new
+ * are both given, as kvinj_append_paged_decode), except that the query of
+ * request r attends to the tokens [max(0, ctx - window), ctx) of its context
+ * only; window == 0 is the whole context. Only blocks holding an attended token
+ * are read, so table entries of pages wholly before the window may hold
+ * anything. Runs the tcgen05 kernel: D = 128, Hkv a multiple of 8, G in
+ * {1, 2, 4, 8}, else KVINJ_EUNSUPPORTED; window < 0 or only one of k_new,
+ * v_new: KVINJ_EINVAL. */
+int kvinj_paged_decode_window(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                              int32_t num_q_heads, const void *q, const void *k_new,
+                              const void *v_new, const int32_t *q_pos,
+                              const int32_t *block_tables, int32_t max_blocks,
+                              const int32_t *context_lens, int32_t batch, int32_t window,
+                              float scale, void *out, void *workspace, size_t ws_bytes,
+                              int32_t *dev_status, kvinj_stream_t stream);
+
 /* Same as kvinj_paged_decode with an explicit kernel choice (G = Hq/Hkv):
  * variant 0 = automatic (3 where it applies, else 2 for G >= 4, else 1),
  * 1 = CUDA-core FMA kernel (G in {1, 2, 4, 8}),

@@ -285,7 +285,7 @@ int decode_call(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
                 const int32_t *q_pos, const int32_t *block_tables, int32_t max_blocks,
                 const int32_t *context_lens, int32_t batch, float scale, void *out,
                 void *workspace, size_t ws_bytes, int32_t *dev_status, kvinj_stream_t stream,
-                int32_t variant, int32_t ctas) {
+                int32_t variant, int32_t ctas, int32_t window = 0) {
   int rc = check_cache(cache, true);
   if (rc) return rc;
   const int D = cache->head_dim, Hkv = cache->num_kv_heads;
@@ -307,6 +307,8 @@ int decode_call(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
   // heads: 61.6 vs 69.6 us per layer for the mma.sync kernel at 8 requests x 8192
   // tokens, 64 q / 8 kv heads), else mma.sync from G = 4 up, else the FMA kernel
   if (variant == 0) variant = umma_ok ? 3 : (G >= 4 ? 2 : 1);
+  if (window < 0) return KVINJ_EINVAL;
+  if (window > 0 && variant != 3) return KVINJ_EUNSUPPORTED;  // the tcgen05 kernel only
   if (variant == 1 && !g_pow2_8) return KVINJ_EUNSUPPORTED;
   if (variant == 2 && !(g_pow2_8 || G == 16)) return KVINJ_EUNSUPPORTED;
   if (variant == 3 && !umma_ok) return KVINJ_EUNSUPPORTED;
@@ -371,6 +373,7 @@ int decode_call(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
   a.layer = layer;
   a.num_blocks = cache->num_blocks;
   a.ctas = ctas;
+  a.window = window;
   const double sc = scale > 0.f ? (double)scale : 1.0 / sqrt((double)D);
   a.scale_log2 = (float)(sc * 1.4426950408889634);
   return cuda_rc(launch_decode(a, tmK, tmV, D, G, HG, cache->dtype, variant, ctas,
@@ -402,6 +405,19 @@ int kvinj_append_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rop
   return decode_call(cache, rope, layer, num_q_heads, q, k_new, v_new, q_pos, block_tables,
                      max_blocks, context_lens, batch, scale, out, workspace, ws_bytes,
                      dev_status, stream, variant, ctas);
+}
+
+int kvinj_paged_decode_window(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                              int32_t num_q_heads, const void *q, const void *k_new,
+                              const void *v_new, const int32_t *q_pos,
+                              const int32_t *block_tables, int32_t max_blocks,
+                              const int32_t *context_lens, int32_t batch, int32_t window,
+                              float scale, void *out, void *workspace, size_t ws_bytes,
+                              int32_t *dev_status, kvinj_stream_t stream) {
+  if ((k_new == nullptr) != (v_new == nullptr)) return KVINJ_EINVAL;
+  return decode_call(cache, rope, layer, num_q_heads, q, k_new, v_new, q_pos, block_tables,
+                     max_blocks, context_lens, batch, scale, out, workspace, ws_bytes,
+                     dev_status, stream, 0, 0, window);
 }
 
 int kvinj_append_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,

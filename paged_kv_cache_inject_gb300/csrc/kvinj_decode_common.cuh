@@ -94,6 +94,7 @@ struct Piece {
   int r, hg;      // request, head group
   int pg0;        // first block (within the request) of this piece
   int ctx;        // context length of the request
+  int lo;         // first token attended to (sliding window; 0 without one)
   int seg_start;  // flattened index of the segment's first unit
   int seg_end;    // one past its last unit
   int end;        // one past this piece's last unit (<= seg_end)
@@ -110,18 +111,29 @@ __device__ __forceinline__ int find_request(const int *pre, int batch, int P) {
   return lo;
 }
 
+// sliding window ("LLM Inference: KV Caching", sliding window attention): a query attends
+// to the last a.window tokens of its context only (a.window == 0: to all of them); the
+// first token attended to
+__device__ __forceinline__ int window_lo(const DecodeArgs &a, int c) {
+  return (a.window > 0 && c > a.window) ? c - a.window : 0;
+}
+
+// the piece of unit P: units of a head group are 16*BPU-token spans of the request's
+// context from the one holding its first attended token
+template <int BPU = 1>
 __device__ __forceinline__ Piece find_piece(const DecodeArgs &a, const int *pre, int ngrp, int P,
                                             int b1) {
   Piece pc;
   pc.r = find_request(pre, a.batch, P);
   const int pages = (pre[pc.r + 1] - pre[pc.r]) / ngrp;
   const int off = P - pre[pc.r];
+  pc.ctx = a.context_lens[pc.r];
+  pc.lo = window_lo(a, pc.ctx);
   pc.hg = off / pages;
-  pc.pg0 = off - pc.hg * pages;
+  pc.pg0 = off - pc.hg * pages + pc.lo / (BLK * BPU);
   pc.seg_start = pre[pc.r] + pc.hg * pages;
   pc.seg_end = pc.seg_start + pages;
   pc.end = min(b1, pc.seg_end);
-  pc.ctx = a.context_lens[pc.r];
   return pc;
 }
 
@@ -170,7 +182,8 @@ __device__ __forceinline__ int context_pages(const DecodeArgs &a, int c) {
 // work units of one head group of a request whose context is c tokens long
 template <int BPU>
 __device__ __forceinline__ int context_units(const DecodeArgs &a, int c) {
-  return (context_pages(a, c) + BPU - 1) / BPU;
+  const int u = (context_pages(a, c) + BPU - 1) / BPU;
+  return u > 0 ? u - window_lo(a, c) / (BLK * BPU) : 0;  // from the first attended token's
 }
 
 // Units per request -> prefix sums pre[0..batch], this CTA's range, barrier
@@ -267,12 +280,17 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
       const int pages = (pre[r + 1] - pre[r]) / ngrp;
       const int off = P - pre[r];
       hg = off / pages;
-      const int pg = off - hg * pages;
+      const int c = __ldg(a.context_lens + r);
+      const int fp = window_lo(a, c) / BLK;  // first page holding an attended token
+      const int pgr = off - hg * pages;
+      const int pg = pgr + fp / Lay::BPU;    // unit index within the request
       rq = r;
-      first = (gi == 0 || pg == 0) ? 1 : 0;  // first unit of a piece
-      blk = a.block_tables[(int64_t)r * a.max_blocks + pg * Lay::BPU];
+      first = (gi == 0 || pgr == 0) ? 1 : 0;  // first unit of a piece
+      // (a two-block unit that starts one page before the window loads the window's first
+      // block in both halves: the page before holds no attended token and is not read)
+      blk = a.block_tables[(int64_t)r * a.max_blocks + max(pg * Lay::BPU, fp)];
       if constexpr (Lay::BPU == 2) {
-        if (pg * 2 + 1 < context_pages(a, __ldg(a.context_lens + r)))
+        if (pg * 2 + 1 < context_pages(a, c))
           blk2 = a.block_tables[(int64_t)r * a.max_blocks + pg * 2 + 1];
       }
       if (Lay::QB && first && a.rope) qp = a.q_pos[r];

@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(256, 1)
       };
       int P = rg.b0, gi0 = 0, piece = 0;
       while (P < rg.b1) {
-        const Piece pc = find_piece(a, pre, ngrp, P, rg.b1);
+        const Piece pc = find_piece<BPU>(a, pre, ngrp, P, rg.b1);
         const int np = pc.end - P, qbuf = piece % QBUF;
         if (wait(qfull + qbuf, (uint32_t)(piece / QBUF) & 1u)) issue_qk(gi0, qbuf);
         if (piece > 0) wait(ofree, (uint32_t)(piece - 1) & 1u);  // O read out
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(256, 1)
     const int *qpos_sm = pre + a.batch + 1;  // copied by the prologue (-1 without RoPE)
     int P = rg.b0, piece = 0;
     while (P < rg.b1) {
-      const Piece pc = find_piece(a, pre, ngrp, P, rg.b1);
+      const Piece pc = find_piece<BPU>(a, pre, ngrp, P, rg.b1);
       const int qbuf = piece % QBUF;
       // the loads (query rows, RoPE row) go out before the wait for the tile
       int qp = a.rope ? qpos_sm[pc.r] : -1;
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(256, 1)
 
     int P = rg.b0, gi0 = 0;
     while (P < rg.b1) {
-      const Piece pc = find_piece(a, pre, ngrp, P, rg.b1);
+      const Piece pc = find_piece<BPU>(a, pre, ngrp, P, rg.b1);
       const int np = pc.end - P;
       float m_run[G], l_part[G];
 #pragma unroll
@@ -404,8 +404,9 @@ __global__ void __launch_bounds__(256, 1)
         const bool ok = wait((Lay::SPLIT_KV ? fullV : full) + st, (uint32_t)(gi / S) & 1u) &&
                         wait(sfull + par, (uint32_t)(gi >> 1) & 1u);
         // this thread's token: in the context and in a block the cache holds
+        const int tok = (pc.pg0 + j) * TPH + t;
         const bool live = ok && ((valid[Lay::SPLIT_KV ? gi % Lay::VR : st] >> (t / BLK)) & 1) &&
-                          (pc.pg0 + j) * TPH + t < pc.ctx;
+                          tok < pc.ctx && tok >= pc.lo;
         float s[G];
         if (ok) {
           tc_fence_after();

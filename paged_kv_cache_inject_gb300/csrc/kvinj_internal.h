@@ -57,6 +57,7 @@ struct DecodeArgs {
   int32_t *status;
   int batch, Hq, Hkv, max_blocks, layer;
   int ctas;                    // split-K grid size (set for the combine pass)
+  int window;                  // sliding window in tokens (0: the whole context)
   int64_t num_blocks;
   float scale_log2;            // softmax scale times log2(e)
 };

@@ -65,6 +65,7 @@ class Engine:
         self.decode_ctas = 0
         self.fused_append = True  # append + decode in one call
         self.overlap_inject = False  # inject on a low-priority stream beside the decode
+        self.window = 0  # sliding window of the decode in tokens (0: whole context)
         self._hi = self._lo = None
 
     # -- single operations ---------------------------------------------------
@@ -83,12 +84,22 @@ class Engine:
                        positions, slots, self.status)
 
     def decode(self, layer, q, q_pos, block_tables, ctx_lens, out, rotate=True):
+        if self.window:
+            K.kvinj_paged_decode_window(self.cache, self.rope if rotate else None, layer, q, q_pos,
+                                        block_tables, ctx_lens, self.window, out, self.workspace,
+                                        status=self.status)
+            return
         K.kvinj_paged_decode_ex(self.cache, self.rope if rotate else None, layer, q, q_pos,
                                 block_tables, ctx_lens, out, self.workspace, 0.0, self.status,
                                 None, self.decode_variant, self.decode_ctas)
 
     def append_decode(self, layer, q, k_new, v_new, q_pos, block_tables, ctx_lens, out,
                       rotate=True):
+        if self.window:
+            K.kvinj_paged_decode_window(self.cache, self.rope if rotate else None, layer, q, q_pos,
+                                        block_tables, ctx_lens, self.window, out, self.workspace,
+                                        k_new=k_new, v_new=v_new, status=self.status)
+            return
         K.kvinj_append_paged_decode(self.cache, self.rope if rotate else None, layer, q, k_new,
                                     v_new, q_pos, block_tables, ctx_lens, out, self.workspace,
                                     0.0, self.status, None, self.decode_variant,

@@ -29,7 +29,7 @@ EXPORTS = [
     "kvinj_append", "kvinj_decode_workspace_size", "kvinj_decode_workspace_init",
     "kvinj_paged_decode", "kvinj_paged_decode_ex", "kvinj_append_paged_decode",
     "kvinj_append_paged_decode_ex", "kvinj_paged_decode_static", "kvinj_kv_bytes",
-    "kvinj_strerror", "kvinj_copy_blocks",
+    "kvinj_strerror", "kvinj_copy_blocks", "kvinj_paged_decode_window",
 ]
 
 
@@ -80,6 +80,9 @@ def load(path: str = LIB_PATH):
             "kvinj_inject": (ctypes.c_int, [P, P, P, P, P, P, i32, i32, i32, P, P]),
             "kvinj_append": (ctypes.c_int, [P, P, i32, P, P, P, P, i64, P, P]),
             "kvinj_copy_blocks": (ctypes.c_int, [P, P, P, i64, i32, i32, P, P]),
+            "kvinj_paged_decode_window": (ctypes.c_int, [P, P, i32, i32, P, P, P, P, P, i32, P,
+                                                         i32, i32, ctypes.c_float, P, P, sz, P,
+                                                         P]),
             "kvinj_decode_workspace_size": (sz, [i32, i32, i32, i32]),
             "kvinj_decode_workspace_init": (ctypes.c_int, [P, sz, P]),
             "kvinj_paged_decode": (ctypes.c_int, [P, P, i32, i32, P, P, P, i32, P, i32,
@@ -238,6 +241,23 @@ def kvinj_copy_blocks(cache: Cache, src, dst, layer_begin: int = 0, layer_end: i
     _check("kvinj_copy_blocks",
            load().kvinj_copy_blocks(cache.ref, _ptr(src), _ptr(dst), src.numel(), layer_begin, le,
                                     _ptr(status), _stream(stream)))
+
+
+def kvinj_paged_decode_window(cache: Cache, rope: Rope | None, layer: int, q, q_pos,
+                              block_tables, context_lens, window: int, out, workspace,
+                              k_new=None, v_new=None, scale: float = 0.0, status=None,
+                              stream=None):
+    """Paged decode over the last `window` tokens of each context (0: all of them), with
+    the new token's append fused when k_new and v_new are given."""
+    batch, Hq, _ = q.shape
+    _check("kvinj_paged_decode_window",
+           load().kvinj_paged_decode_window(
+               cache.ref, rope.ref if rope is not None else None, layer, Hq, _ptr(q),
+               _ptr(k_new) if k_new is not None else None,
+               _ptr(v_new) if v_new is not None else None, _ptr(q_pos), _ptr(block_tables),
+               block_tables.shape[1], _ptr(context_lens), batch, window, float(scale), _ptr(out),
+               _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+               _stream(stream)))
 
 
 def kvinj_append(cache: Cache, rope: Rope | None, layer: int, k_new, v_new, positions,

@@ -604,6 +604,82 @@ def test_decode_umma_refuses_shapes_it_does_not_cover():
 
 
 # ---------------------------------------------------------------------------
+# sliding-window decode (tcgen05 kernel)
+# ---------------------------------------------------------------------------
+def _run_window(kc, vc, q, bt, ctx, window, dt, theta, rope_max, kn=None, vn=None, status=None):
+    tdt = torch_dtype(dt)
+    D = kc.shape[-1]
+    cache = K.Cache(from_bits(kc, tdt), from_bits(vc, tdt))
+    rope = K.make_rope(theta, D, rope_max)
+    batch, Hq, _ = q.shape
+    ws = K.make_decode_workspace(batch, Hq, kc.shape[2], D)
+    out = torch.full((batch, Hq, D), float("nan"), dtype=tdt, device="cuda")
+    K.kvinj_paged_decode_window(cache, rope, 1, from_bits(q, tdt), i32(ctx - 1), i32(bt), i32(ctx),
+                                window, out, ws,
+                                k_new=None if kn is None else from_bits(kn, tdt),
+                                v_new=None if vn is None else from_bits(vn, tdt), status=status)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64), cache
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("window", [1, 16, 37, 100, 1000])
+def test_decode_window_matches_oracle(G, window):
+    dt, theta = W.BF16, 5e5
+    ctx = np.array([1, 16, 17, 250, 611, 33], np.int32)
+    kc, vc, q, bt = _decode_case(128, G, dt, ctx, Hkv=8, L=2, seed=60 + G)
+    status = status_tensor()
+    got, _ = _run_window(kc, vc, q, bt, ctx, window, dt, theta, 700, status=status)
+    assert status.item() == 0
+    want, st = oracle.paged_decode(kc, vc, 1, q, ctx - 1, bt, ctx, theta, dt, window=window)
+    assert st == 0
+    assert_decode_close(got, want, f"window {window} G{G}")
+
+
+@pytest.mark.parametrize("G", [4, 8])
+def test_decode_window_ignores_pages_before_it(G):
+    # table entries of pages wholly before the window are never read (here: -1), and a
+    # two-block unit that starts one page before the window still sees the right tokens
+    dt, theta = W.BF16, 5e5
+    ctx = np.array([611, 250, 1000], np.int32)
+    kc, vc, q, bt = _decode_case(128, G, dt, ctx, Hkv=8, L=2, seed=70 + G)
+    window = 150  # first attended tokens 461, 100, 850: pages 28, 6, 53 (even and odd)
+    bt2 = bt.copy()
+    for r, c in enumerate(ctx):
+        bt2[r, : (c - window) // 16] = -1
+    status = status_tensor()
+    got, _ = _run_window(kc, vc, q, bt2, ctx, window, dt, theta, 1100, status=status)
+    assert status.item() == 0
+    want, st = oracle.paged_decode(kc, vc, 1, q, ctx - 1, bt2, ctx, theta, dt, window=window)
+    assert st == 0
+    assert_decode_close(got, want, f"window before-pages G{G}")
+
+
+def test_decode_window_fused_append_and_refusals():
+    D, G, dt, Hkv, theta = 128, 4, W.BF16, 8, 5e5
+    ctx = np.array([700, 33, 1500, 16], np.int32)
+    kc, vc, q, bt, kn, vn, ctx, pos, slots, theta, ek, ev, _ = _fused_case(D, G, dt, list(ctx),
+                                                                         Hkv, seed=77)
+    want, st = oracle.paged_decode(ek, ev, 1, q, pos, bt, ctx, theta, dt, window=200)
+    assert st == 0
+    status = status_tensor()
+    got, cache = _run_window(kc, vc, q, bt, ctx, 200, dt, theta, int(ctx.max()) + 4, kn=kn, vn=vn,
+                             status=status)
+    assert status.item() == 0
+    assert np.array_equal(bits(cache.v), ev) and ulp_distance(bits(cache.k), ek).max() <= 1
+    assert_decode_close(got, want, "window + fused append")
+    # shapes the tcgen05 kernel does not take, and bad arguments
+    for D2, G2, Hkv2 in [(64, 4, 8), (128, 16, 8), (128, 4, 4)]:
+        k2, v2, q2, bt2 = _decode_case(D2, G2, dt, [40], Hkv=Hkv2, L=2, seed=78)
+        with pytest.raises(K.KvinjError) as e:
+            _run_window(k2, v2, q2, bt2, np.array([40], np.int32), 8, dt, theta, 64)
+        assert e.value.code == K.KVINJ_EUNSUPPORTED
+    with pytest.raises(K.KvinjError) as e:
+        _run_window(kc, vc, q, bt, ctx, -1, dt, theta, int(ctx.max()) + 4)
+    assert e.value.code == K.KVINJ_EINVAL
+
+
+# ---------------------------------------------------------------------------
 # append + decode in one call
 # ---------------------------------------------------------------------------
 def _fused_case(D, G, dt, ctx, Hkv, seed, rotate=True):

@@ -32,7 +32,7 @@ def _worker(rank, world, port, q):
         cfg = W.CONFIGS["llama3_8b_b32"]
         wl = W.make_workload(cfg, seed=bench.replica_seed(cfg.seed, rank))
         # the reference arm: rank 0 alone prints its line, the others exit at once
-        args = types.SimpleNamespace(config="tiny_1layer", steps=1, warmup=0)
+        args = types.SimpleNamespace(config="tiny_1layer", steps=1, warmup=0, window=0)
         buf = io.StringIO()
         with contextlib.redirect_stdout(buf):
             bench.run_reference(args)

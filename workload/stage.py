@@ -96,14 +96,15 @@ def pinned_copy(inp: StepInputs) -> StepInputs:
     return StepInputs(*[t.cpu().pin_memory() for t in inp.tensors()])
 
 
-def algorithmic_bytes(wl: Workload) -> dict:
+def algorithmic_bytes(wl: Workload, window: int = 0) -> dict:
     """Bytes one step must move at minimum, per part (the roofline numerator).
 
     inject: read the injected chunks' K/V rows and write them to the cache,
             2 * (2 * L * Hkv * D * b) per injected token;
     append: the same per new token and layer, read + write;
-    decode: read every context token's K and V once per layer and step,
-            plus q, out and the block-table entries of the pages read."""
+    decode: read every context token's K and V once per layer and step (under a sliding
+            window of `window` tokens only the last `window`), plus q, out and the
+            block-table entries of the pages read."""
     cfg = wl.cfg
     b = cfg.elem_bytes
     row = cfg.kv_heads * cfg.head_dim * b
@@ -113,8 +114,9 @@ def algorithmic_bytes(wl: Workload) -> dict:
     decode = 0
     for s in range(cfg.steps):
         ctx = wl.context_lens.astype(np.int64) + s + 1
-        pages = -(-ctx // cfg.block_size)
-        kv_bytes = int(ctx.sum()) * 2 * row
+        lo = np.maximum(ctx - window, 0) if window > 0 else np.zeros_like(ctx)
+        pages = -(-ctx // cfg.block_size) - lo // cfg.block_size
+        kv_bytes = int((ctx - lo).sum()) * 2 * row
         small = cfg.batch * cfg.q_heads * cfg.head_dim * b * 2 + int(pages.sum()) * 4
         decode += cfg.layers * (kv_bytes + small)
     return {"inject": inject, "append": append, "decode": decode,
