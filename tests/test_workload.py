@@ -79,3 +79,25 @@ def test_workload_sizes_match_the_shapes():
     assert abs(cfg.pool_bytes / 1e9 - 34.36) < 0.01
     assert abs(W.CONFIGS["llama3_70b_b8_8k"].pool_bytes / 1e9 - 171.80) < 0.01
     assert abs(W.CONFIGS["mixed_b64_loguniform"].pool_bytes / 1e9 - 209.72) < 0.01
+
+
+def test_algorithmic_bytes_under_a_window():
+    # under a sliding window of W tokens a decode call reads the K and V of the last
+    # min(ctx, W) tokens of each context and the table entries of the pages holding them;
+    # a window longer than every context counts the same bytes as none
+    from workload import stage
+    wl = W.make_workload(W.CONFIGS["llama3_70b_b8_8k"])
+    cfg = wl.cfg
+    full = stage.algorithmic_bytes(wl)
+    assert stage.algorithmic_bytes(wl, 10 ** 6) == full
+    win = stage.algorithmic_bytes(wl, 4096)
+    row = cfg.kv_heads * cfg.head_dim * 2
+    small = cfg.batch * cfg.q_heads * cfg.head_dim * 2 * 2
+    want = 0
+    for s in range(cfg.steps):
+        c = 8192 + s + 1  # fixed contexts, plus the tokens appended by steps 0..s
+        pages = -(-c // 16) - (c - 4096) // 16
+        want += cfg.layers * (cfg.batch * (4096 * 2 * row + pages * 4) + small)
+    assert win["decode"] == want
+    assert win["inject"] == full["inject"] and win["append"] == full["append"]
+    assert win["total"] == win["inject"] + win["append"] + win["decode"]
