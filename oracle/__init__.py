@@ -1,7 +1,7 @@
 """fp64 CPU oracle for the paged KV-injection path -- TEST INFRASTRUCTURE.
 
 A plain, slow statement of what the path computes (RoPE, slot mapping,
-inject, append, block copies, paged decode attention), written in C in ``kvinj_oracle.c``
+inject, append, block copies, paged decode attention, paged prefill of query tokens), written in C in ``kvinj_oracle.c``
 and wrapped here with ctypes over numpy arrays. It shares no code with the
 CUDA library in ``paged_kv_cache_inject_gb300``, and neither imports the
 other. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg
@@ -78,6 +78,10 @@ def _load():
                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
                                            ctypes.c_int, f64, P, ctypes.c_int, P, ctypes.c_int,
                                            f64, P, ctypes.c_int, ctypes.c_int]),
+                "orc_paged_prefill": (i32, [P, P, ctypes.c_int, ctypes.c_int, i64, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, i64,
+                                            f64, P, ctypes.c_int, ctypes.c_int, f64, P,
+                                            ctypes.c_int]),
                 "orc_has_openmp": (ctypes.c_int, []),
             }
             for name, (res, args) in sig.items():
@@ -236,6 +240,24 @@ def attention_bits(q_bits, q_pos, theta, K_bits, V_bits, dtype, scale=0.0, rotat
     _load().orc_attention_bits(_p(qb), int(rotate_q), float(q_pos), float(theta), _p(Kb),
                                _p(Vb), n, D, dtype, float(scale), _p(out))
     return out
+
+
+def paged_prefill(k_cache, v_cache, layer, q_bits, seq_ids, positions, block_tables, theta,
+                  dtype, scale=0.0, n_threads=1):
+    """Query tokens q_bits[n][Hq][D] of requests seq_ids[n] at positions[n], each attending
+    causally to its request's tokens 0..position (already in the cache); returns (out fp64
+    [n][Hq][D], status)."""
+    L, NB, Hkv, B, D = k_cache.shape
+    q = _c(q_bits, np.uint16)
+    n, Hq, _ = q.shape
+    sq = _c(seq_ids, np.int32)
+    ps = _c(positions, np.int32)
+    bt = _c(block_tables, np.int32)
+    out = np.empty((n, Hq, D), np.float64)
+    st = _load().orc_paged_prefill(_p(k_cache), _p(v_cache), Hkv, D, NB, B, dtype, layer, Hq,
+                                   _p(q), _p(sq), _p(ps), n, float(theta), _p(bt), bt.shape[1],
+                                   bt.shape[0], float(scale), _p(out), n_threads)
+    return out, int(st)
 
 
 def paged_decode(k_cache, v_cache, layer, q_bits, q_pos, block_tables, context_lens, theta,

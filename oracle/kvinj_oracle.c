@@ -378,6 +378,52 @@ int32_t orc_paged_decode(const uint16_t *k_cache, const uint16_t *v_cache, int H
   return st;
 }
 
+/* ------------------------------------------------------------------ */
+/* Paged prefill of the query tokens over the injected cache [IS §3.4  */
+/* step 4: only the query tokens are prefilled, attending to the       */
+/* injected memory as if it had been prefilled]. Query token i belongs */
+/* to request seq[i] and sits at position pos[i]; its K/V are already  */
+/* in the cache (write, then attend) and it attends causally to the    */
+/* request's tokens 0..pos[i]: out[i][qh] = attention of q[i][qh]       */
+/* (rotated at pos[i]) over those keys of kv head qh / G.               */
+/* ------------------------------------------------------------------ */
+int32_t orc_paged_prefill(const uint16_t *k_cache, const uint16_t *v_cache, int Hkv, int D,
+                          int64_t num_blocks, int B, int dtype, int layer, int Hq,
+                          const uint16_t *q, const int32_t *seq, const int32_t *pos, int64_t n,
+                          double theta, const int32_t *block_tables, int max_blocks, int batch,
+                          double scale, double *out, int n_threads) {
+  int32_t st = 0;
+  int G = Hq / Hkv;
+  if (scale <= 0.0) scale = 1.0 / sqrt((double)D);
+#pragma omp parallel for num_threads(n_threads) reduction(| : st) schedule(dynamic)
+  for (int64_t iq = 0; iq < n * Hq; ++iq) {
+    int64_t i = iq / Hq;
+    int qh = (int)(iq % Hq), h = qh / G;
+    double *o = out + iq * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    int r = seq[i];
+    int64_t ctx = (int64_t)pos[i] + 1;
+    if (r < 0 || r >= batch) { st |= ORC_ST_SEQ; continue; }
+    if (pos[i] < 0 || ctx > (int64_t)max_blocks * B) { st |= ORC_ST_POS; continue; }
+    uint16_t *Kr = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)ctx * D);
+    uint16_t *Vr = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)ctx * D);
+    int bad = 0;
+    for (int64_t j = 0; j < ctx; ++j) {
+      int32_t page_blk = block_tables[(int64_t)r * max_blocks + j / B];
+      if (page_blk < 0 || page_blk >= num_blocks) { bad = 1; break; }
+      int64_t src = cache_row(layer, (int64_t)page_blk * B + j % B, h, num_blocks, Hkv, B, D);
+      memcpy(Kr + j * D, k_cache + src, sizeof(uint16_t) * D);
+      memcpy(Vr + j * D, v_cache + src, sizeof(uint16_t) * D);
+    }
+    if (bad) st |= ORC_ST_BLOCK;
+    else
+      orc_attention_bits(q + iq * D, 1, (double)pos[i], theta, Kr, Vr, ctx, D, dtype, scale, o);
+    free(Kr);
+    free(Vr);
+  }
+  return st;
+}
+
 int orc_has_openmp(void) {
 #ifdef _OPENMP
   return 1;

@@ -43,6 +43,9 @@ MUTANTS = [
      "for (int l = l0; l < l0 + 1; ++l)\n      for (int h = 0; h < Hkv; ++h)\n        for (int t = 0; t < B; ++t) {"),
     ("window_off_by_one", "int64_t j0 = (window > 0 && ctx > window) ? ctx - window : 0",
      "int64_t j0 = (window > 0 && ctx > window) ? ctx - window + 1 : 0"),
+    ("prefill_excludes_itself", "    int64_t ctx = (int64_t)pos[i] + 1;\n    if (r < 0",
+     "    int64_t ctx = (int64_t)pos[i];\n    if (r < 0"),
+    ("prefill_first_request_table", "    int r = seq[i];\n", "    int r = 0;\n"),
     ("copy_blocks_k_only", "            v_cache[to + d] = v_cache[from + d];\n", ""),
 ]
 

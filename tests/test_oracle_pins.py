@@ -419,6 +419,57 @@ def test_sliding_window_decode():
     assert st == 0 and np.array_equal(out, want)
 
 
+def test_paged_prefill_is_causal_attention_over_memory_and_query():
+    # only the query tokens are prefilled, attending to the injected memory as if it had been
+    # prefilled ("InferScale" §3.4 step 4): query token i at position p attends to tokens 0..p
+    # of its request (memory, earlier query tokens, itself); checked against textbook
+    # attention on contiguous arrays, two requests interleaved in the token list
+    rng = np.random.default_rng(29)
+    B, NB, Hkv, G, D, theta = 16, 20, 2, 2, 64, 5e5
+    Hq = Hkv * G
+    mem, nq = [40, 7], [5, 9]  # memory tokens and query tokens per request
+    total = [m + n for m, n in zip(mem, nq)]
+    Ks = [oracle.encode(rng.standard_normal((t, Hkv, D)), BF16) for t in total]
+    Vs = [oracle.encode(rng.standard_normal((t, Hkv, D)), BF16) for t in total]
+    perm = rng.permutation(NB).astype(np.int32)
+    bt = np.full((2, 5), -1, np.int32)
+    kc = np.zeros((1, NB, Hkv, B, D), np.uint16)
+    vc = np.zeros_like(kc)
+    o = 0
+    for r, t in enumerate(total):
+        pages = -(-t // B)
+        bt[r, :pages] = perm[o:o + pages]
+        o += pages
+        for p in range(t):
+            kc[0, bt[r, p // B], :, p % B] = Ks[r][p]
+            vc[0, bt[r, p // B], :, p % B] = Vs[r][p]
+    toks = [(r, mem[r] + i) for i in range(max(nq)) for r in range(2) if i < nq[r]]
+    seq = np.array([t[0] for t in toks], np.int32)
+    pos = np.array([t[1] for t in toks], np.int32)
+    q = oracle.encode(rng.standard_normal((len(toks), Hq, D)), BF16)
+    out, st = oracle.paged_prefill(kc, vc, 0, q, seq, pos, bt, theta, BF16)
+    assert st == 0
+    for i, (r, p) in enumerate(toks):
+        for qh in range(Hq):
+            h = qh // G
+            want = oracle.attention_bits(q[i, qh], p, theta, Ks[r][: p + 1, h], Vs[r][: p + 1, h],
+                                         BF16)
+            assert np.array_equal(out[i, qh], want)
+    # causal: a later token's key changes later outputs only
+    kc2 = kc.copy()
+    r, p = 1, mem[1] + 4
+    kc2[0, bt[r, p // B], :, p % B] ^= 0x0040
+    out2, _ = oracle.paged_prefill(kc2, vc, 0, q, seq, pos, bt, theta, BF16)
+    for i, (ri, pi) in enumerate(toks):
+        same = np.array_equal(out2[i], out[i])
+        assert same == (ri != r or pi < p), (ri, pi)
+    # a position past the table or a request outside the batch is flagged
+    _, st = oracle.paged_prefill(kc, vc, 0, q[:1], [0], [5 * B], bt, theta, BF16)
+    assert st == 8
+    _, st = oracle.paged_prefill(kc, vc, 0, q[:1], [2], [3], bt, theta, BF16)
+    assert st == 32
+
+
 def test_gqa_groups_are_consecutive_query_heads():
     # "groups of four share one key and value head" ("LLM Inference: KV Caching");
     # reading: query heads g*G .. g*G+G-1 use kv head g
