@@ -43,6 +43,15 @@
 // 2^TAU), and O and l are rescaled only when m moves. The final
 // O / l is the same quotient as with an always-current maximum.
 //
+// At G = 8 the K and V halves of a stage have their own barrier pairs: K is released by a
+// commit after its QK, V after its PV, so the next units' K can land while this unit's
+// softmax runs; the softmax waits on the V half (the K half's barrier may already be phases
+// ahead), and the block valid bits sit in a ring deep enough for that lead.
+//
+// Sliding window (a.window > 0): a request's units start at the one holding its first
+// attended token (context length minus the window); the softmax masks tokens before it as
+// it masks those past the context.
+//
 // Warp roles (256 threads):
 //   warp 0     TMA producer (stages of K and V rows)
 //   warp 1     TMEM owner; lane 0 issues every MMA and commit
