@@ -427,6 +427,22 @@ def run_gpu(args):
     copy_bytes = 2 * 2 * n_copy * cfg.layers * rec_bytes  # K and V, read and write
     copy_avg = part_ms(lambda: eng.copy_blocks(copy_ids, copy_ids), max(3, args.steps))
     copy_gbs = copy_bytes / (copy_avg * 1e-3) / 1e9
+    # paged prefill: the last nq tokens of every context taken as layer 0's query tokens (their
+    # K/V are in the cache); each token is a decode row over its own causal context
+    import numpy as np
+    ctx_h = wl.context_lens.astype(np.int64) + 1
+    nq = int(min(16, ctx_h.min()))
+    pos_h = (ctx_h[:, None] - nq + np.arange(nq)[None, :]).reshape(-1)
+    pf_seq = torch.from_numpy(np.repeat(np.arange(cfg.batch), nq).astype(np.int32)).to(dev)
+    pf_pos = torch.from_numpy(pos_h.astype(np.int32)).to(dev)
+    pf_q = inp.q[0, 0].repeat_interleave(nq, dim=0).contiguous()
+    pf_out = torch.empty_like(pf_q)
+    eng.prefill(0, pf_q, pf_seq, pf_pos, inp.block_tables, pf_out)  # workspace allocated here
+    pf_avg = part_ms(lambda: eng.prefill(0, pf_q, pf_seq, pf_pos, inp.block_tables, pf_out),
+                     max(3, args.steps))
+    kv_row = cfg.kv_heads * cfg.head_dim * cfg.elem_bytes
+    pf_read = int((pos_h + 1).sum()) * 2 * kv_row
+    pf_unique = int(ctx_h.sum()) * 2 * kv_row
     peak, peak_kind = _peaks()
     # slot mapping, inject (one launch, or one per layer when overlapped), then per step and
     # layer the append + decode launches
@@ -498,6 +514,12 @@ def run_gpu(args):
                        "pct_of_8tbs": 100 * dec_gbs / NOMINAL_HBM_GBS,
                        "tokens_per_s": ws * cfg.batch * cfg.steps / (ms_step * 1e-3),
                        "bytes_per_launch": per_launch_decode},
+            "prefill": {"query_tokens": int(pos_h.size), "per_request": nq, "layers": 1,
+                        "ms": pf_avg, "tokens_per_s": pos_h.size / (pf_avg * 1e-3),
+                        "kv_bytes_read": pf_read, "gbs": pf_read / (pf_avg * 1e-3) / 1e9,
+                        "unique_kv_bytes": pf_unique,
+                        "note": "each query token a decode row over its causal context; "
+                                "unique bytes are each request's context read once"},
             "copy_blocks": {"blocks": n_copy, "layers": cfg.layers, "bytes": copy_bytes,
                             "ms": copy_avg, "gbs": copy_gbs,
                             "note": "each block copied onto itself: full reads and writes, "

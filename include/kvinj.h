@@ -215,6 +215,29 @@ int kvinj_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t
                        void *workspace, size_t ws_bytes, int32_t *dev_status,
                        kvinj_stream_t stream);
 
+/* Paged prefill of query tokens over the injected cache ("InferScale" §3.4 step
+ * 4: only the query tokens are prefilled, attending to the injected memory as
+ * if it had been prefilled). Query token i < n of request seq_ids[i] sits at
+ * positions[i]; its K/V must already be in the cache (kvinj_append), and it
+ * attends causally to the request's tokens 0..positions[i]: out[i][qh] =
+ * softmax(scale * q' . K) V over those tokens of kv head qh / G, q' = q[i][qh]
+ * rotated at positions[i] (as given when rope == NULL). q, out: device
+ * [n][num_q_heads][D] in the cache dtype; seq_ids, positions: device int32 [n];
+ * block_tables: device int32 [batch][max_blocks]. The tokens are computed as
+ * decode rows (context positions[i] + 1 under the request's table), in launches
+ * of up to 1024 tokens: every row reads its own causal context. workspace:
+ * device, kvinj_prefill_workspace_size() bytes, 16-byte aligned, any contents.
+ * A request id outside [0, batch) or a position outside the table gives a zero
+ * output row, KVINJ_ST_BAD_SEQ or KVINJ_ST_BAD_POS, and KVINJ_ST_BAD_CTX. */
+size_t kvinj_prefill_workspace_size(int32_t n, int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t max_blocks);
+int kvinj_paged_prefill(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                        int32_t num_q_heads, const void *q, const int32_t *seq_ids,
+                        const int32_t *positions, int32_t n, const int32_t *block_tables,
+                        int32_t max_blocks, int32_t batch, float scale, void *out,
+                        void *workspace, size_t ws_bytes, int32_t *dev_status,
+                        kvinj_stream_t stream);
+
 /* Paged decode under a sliding window ("LLM Inference: KV Caching", sliding
  * window attention: a token attends only to the last W tokens). As
  * kvinj_paged_decode (with the new token's append fused when k_new and v_new

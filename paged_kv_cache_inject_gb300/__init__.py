@@ -8,6 +8,7 @@ from .kvinj import (  # noqa: F401
     Cache, KvinjError, Pool, Rope, kvinj_append, kvinj_append_paged_decode, kvinj_copy_blocks,
     kvinj_decode_workspace_init,
     kvinj_decode_workspace_size, kvinj_inject, kvinj_kv_bytes, kvinj_paged_decode,
-    kvinj_paged_decode_ex, kvinj_paged_decode_static, kvinj_paged_decode_window, kvinj_rope_table_bytes, kvinj_rope_table_host, kvinj_slot_mapping,
+    kvinj_paged_decode_ex, kvinj_paged_decode_static, kvinj_paged_decode_window,
+    kvinj_paged_prefill, kvinj_prefill_workspace_size, make_prefill_workspace, kvinj_rope_table_bytes, kvinj_rope_table_host, kvinj_slot_mapping,
     kvinj_strerror, make_decode_workspace, make_rope,
 )

@@ -407,6 +407,59 @@ int kvinj_append_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rop
                      dev_status, stream, variant, ctas);
 }
 
+// query tokens per decode launch of a prefill
+constexpr int PREFILL_CHUNK = 1024;
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t kvinj_prefill_workspace_size(int32_t n, int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t max_blocks) {
+  if (n <= 0 || max_blocks <= 0) return 0;
+  const size_t dec = kvinj_decode_workspace_size(1, num_q_heads, num_kv_heads, head_dim);
+  if (!dec) return 0;
+  const size_t rows = (size_t)(n < PREFILL_CHUNK ? n : PREFILL_CHUNK);
+  return align256(dec) + align256(rows * max_blocks * 4) + 2 * align256(rows * 4);
+}
+
+int kvinj_paged_prefill(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
+                        int32_t num_q_heads, const void *q, const int32_t *seq_ids,
+                        const int32_t *positions, int32_t n, const int32_t *block_tables,
+                        int32_t max_blocks, int32_t batch, float scale, void *out,
+                        void *workspace, size_t ws_bytes, int32_t *dev_status,
+                        kvinj_stream_t stream) {
+  int rc = check_cache(cache, true);
+  if (rc) return rc;
+  if (n < 0 || batch < 0 || max_blocks <= 0 || num_q_heads <= 0) return KVINJ_EINVAL;
+  if (n == 0) return KVINJ_OK;
+  if (!q || !seq_ids || !positions || !block_tables || !out || !workspace) return KVINJ_EINVAL;
+  if (!aligned16(workspace)) return KVINJ_EINVAL;
+  const size_t need = kvinj_prefill_workspace_size(n, num_q_heads, cache->num_kv_heads,
+                                                   cache->head_dim, max_blocks);
+  if (!need) return KVINJ_EINVAL;
+  if (ws_bytes < need) return KVINJ_EWORKSPACE;
+  const size_t dec = align256(kvinj_decode_workspace_size(1, num_q_heads, cache->num_kv_heads,
+                                                          cache->head_dim));
+  const int chunk = n < PREFILL_CHUNK ? n : PREFILL_CHUNK;
+  char *w = static_cast<char *>(workspace);
+  int32_t *row_bt = reinterpret_cast<int32_t *>(w + dec);
+  int32_t *row_ctx = reinterpret_cast<int32_t *>(w + dec + align256((size_t)chunk * max_blocks * 4));
+  int32_t *row_qpos = row_ctx + align256((size_t)chunk * 4) / 4;
+  const size_t row_bytes = (size_t)num_q_heads * cache->head_dim * 2;
+  for (int32_t i0 = 0; i0 < n; i0 += chunk) {
+    const int rows = (n - i0) < chunk ? (n - i0) : chunk;
+    rc = cuda_rc(launch_prefill_rows(block_tables, max_blocks, batch, cache->block_size, seq_ids,
+                                     positions, i0, rows, row_bt, row_ctx, row_qpos, dev_status,
+                                     (cudaStream_t)stream));
+    if (rc) return rc;
+    rc = decode_call(cache, rope, layer, num_q_heads,
+                     static_cast<const char *>(q) + (size_t)i0 * row_bytes, nullptr, nullptr,
+                     row_qpos, row_bt, max_blocks, row_ctx, rows, scale,
+                     static_cast<char *>(out) + (size_t)i0 * row_bytes, workspace, dec, dev_status,
+                     stream, 0, 0);
+    if (rc) return rc;
+  }
+  return KVINJ_OK;
+}
+
 int kvinj_paged_decode_window(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
                               int32_t num_q_heads, const void *q, const void *k_new,
                               const void *v_new, const int32_t *q_pos,

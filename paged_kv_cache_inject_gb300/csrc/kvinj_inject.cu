@@ -328,4 +328,48 @@ cudaError_t launch_copy_blocks(const CopyBlocksArgs &a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// paged prefill: decode rows of query tokens
+// ---------------------------------------------------------------------------
+// "InferScale" §3.4 step 4: the query tokens are prefilled over the injected memory. Query
+// token i of request r at position p (its K/V already in the cache) attends to r's tokens
+// 0..p, which is the decode of a row whose context is p + 1 tokens under r's block table.
+// One thread per entry of the rows' tables; the thread of page 0 also writes the row's
+// context length and q position.
+__global__ void prefill_rows_kernel(const int32_t *__restrict__ bt, int max_blocks, int batch,
+                                    int B, const int32_t *__restrict__ seq,
+                                    const int32_t *__restrict__ pos, int64_t i0, int rows,
+                                    int32_t *row_bt, int32_t *row_ctx, int32_t *row_qpos,
+                                    int32_t *status) {
+  int bad = 0;
+  const int64_t total = (int64_t)rows * max_blocks;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int i = (int)(e / max_blocks), pg = (int)(e % max_blocks);
+    const int r = seq[i0 + i], p = pos[i0 + i];
+    const bool ok_r = r >= 0 && r < batch;
+    row_bt[e] = ok_r ? bt[(int64_t)r * max_blocks + pg] : -1;
+    if (pg == 0) {
+      const bool ok_p = p >= 0 && (int64_t)p < (int64_t)max_blocks * B;
+      if (!ok_r) bad |= KVINJ_ST_BAD_SEQ;
+      else if (!ok_p) bad |= KVINJ_ST_BAD_POS;
+      row_ctx[i] = (ok_r && ok_p) ? p + 1 : 0;
+      row_qpos[i] = (ok_r && ok_p) ? p : 0;
+    }
+  }
+  if (bad) report(status, bad);
+}
+
+cudaError_t launch_prefill_rows(const int32_t *bt, int max_blocks, int batch, int B,
+                                const int32_t *seq, const int32_t *pos, int64_t i0, int rows,
+                                int32_t *row_bt, int32_t *row_ctx, int32_t *row_qpos,
+                                int32_t *status, cudaStream_t s) {
+  int64_t ctas = ((int64_t)rows * max_blocks + 255) / 256;
+  const int64_t cap = (int64_t)num_sms() * 8;
+  if (ctas > cap) ctas = cap;
+  prefill_rows_kernel<<<(int)(ctas < 1 ? 1 : ctas), 256, 0, s>>>(
+      bt, max_blocks, batch, B, seq, pos, i0, rows, row_bt, row_ctx, row_qpos, status);
+  return cudaGetLastError();
+}
+
 }  // namespace kvinj

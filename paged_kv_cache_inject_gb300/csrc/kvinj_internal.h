@@ -84,6 +84,13 @@ struct CopyBlocksArgs {
   int32_t *status;
 };
 cudaError_t launch_copy_blocks(const CopyBlocksArgs &a, cudaStream_t s);
+
+// paged prefill as decode rows: row i of a chunk is query token i0 + i, with its request's
+// block-table row, context length position + 1 (0 when the token is invalid) and q position
+cudaError_t launch_prefill_rows(const int32_t *bt, int max_blocks, int batch, int B,
+                                const int32_t *seq, const int32_t *pos, int64_t i0, int rows,
+                                int32_t *row_bt, int32_t *row_ctx, int32_t *row_qpos,
+                                int32_t *status, cudaStream_t s);
 // HG: kv heads per work unit (a power of two <= 8 dividing Hkv)
 int decode_head_group(int Hkv);
 cudaError_t launch_decode_ffma(const DecodeArgs &a, const CUtensorMap &tmK,

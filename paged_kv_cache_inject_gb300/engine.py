@@ -66,6 +66,7 @@ class Engine:
         self.fused_append = True  # append + decode in one call
         self.overlap_inject = False  # inject on a low-priority stream beside the decode
         self.window = 0  # sliding window of the decode in tokens (0: whole context)
+        self._prefill_ws = None
         self._hi = self._lo = None
 
     # -- single operations ---------------------------------------------------
@@ -104,6 +105,16 @@ class Engine:
                                     v_new, q_pos, block_tables, ctx_lens, out, self.workspace,
                                     0.0, self.status, None, self.decode_variant,
                                     self.decode_ctas)
+
+    def prefill(self, layer, q, seq_ids, positions, block_tables, out, rotate=True):
+        """Query tokens q[n] of requests seq_ids[n] at positions[n] (K/V already appended),
+        each attending causally to its request's tokens 0..position."""
+        need = K.kvinj_prefill_workspace_size(q.shape[0], self.Hq, self.Hkv, self.D,
+                                              block_tables.shape[1])
+        if self._prefill_ws is None or self._prefill_ws.numel() < need:
+            self._prefill_ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        K.kvinj_paged_prefill(self.cache, self.rope if rotate else None, layer, q, seq_ids,
+                              positions, block_tables, out, self._prefill_ws, status=self.status)
 
     def copy_blocks(self, src: torch.Tensor, dst: torch.Tensor, layer_begin: int = 0,
                     layer_end: int | None = None):

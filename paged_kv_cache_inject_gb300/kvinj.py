@@ -30,6 +30,7 @@ EXPORTS = [
     "kvinj_paged_decode", "kvinj_paged_decode_ex", "kvinj_append_paged_decode",
     "kvinj_append_paged_decode_ex", "kvinj_paged_decode_static", "kvinj_kv_bytes",
     "kvinj_strerror", "kvinj_copy_blocks", "kvinj_paged_decode_window",
+    "kvinj_prefill_workspace_size", "kvinj_paged_prefill",
 ]
 
 
@@ -80,6 +81,9 @@ def load(path: str = LIB_PATH):
             "kvinj_inject": (ctypes.c_int, [P, P, P, P, P, P, i32, i32, i32, P, P]),
             "kvinj_append": (ctypes.c_int, [P, P, i32, P, P, P, P, i64, P, P]),
             "kvinj_copy_blocks": (ctypes.c_int, [P, P, P, i64, i32, i32, P, P]),
+            "kvinj_prefill_workspace_size": (sz, [i32, i32, i32, i32, i32]),
+            "kvinj_paged_prefill": (ctypes.c_int, [P, P, i32, i32, P, P, P, i32, P, i32, i32,
+                                                   ctypes.c_float, P, P, sz, P, P]),
             "kvinj_paged_decode_window": (ctypes.c_int, [P, P, i32, i32, P, P, P, P, P, i32, P,
                                                          i32, i32, ctypes.c_float, P, P, sz, P,
                                                          P]),
@@ -258,6 +262,33 @@ def kvinj_paged_decode_window(cache: Cache, rope: Rope | None, layer: int, q, q_
                block_tables.shape[1], _ptr(context_lens), batch, window, float(scale), _ptr(out),
                _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
                _stream(stream)))
+
+
+def kvinj_prefill_workspace_size(n: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                                 max_blocks: int) -> int:
+    return int(load().kvinj_prefill_workspace_size(n, num_q_heads, num_kv_heads, head_dim,
+                                                   max_blocks))
+
+
+def make_prefill_workspace(n, num_q_heads, num_kv_heads, head_dim, max_blocks, device="cuda"):
+    nbytes = kvinj_prefill_workspace_size(n, num_q_heads, num_kv_heads, head_dim, max_blocks)
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def kvinj_paged_prefill(cache: Cache, rope: Rope | None, layer: int, q, seq_ids, positions,
+                        block_tables, out, workspace, scale: float = 0.0, status=None,
+                        stream=None):
+    """Query tokens q[n][Hq][D] of requests seq_ids[n] at positions[n] (their K/V already in
+    the cache), each attending causally to its request's tokens 0..position."""
+    n, Hq, _ = q.shape
+    _check("kvinj_paged_prefill",
+           load().kvinj_paged_prefill(cache.ref, rope.ref if rope is not None else None, layer,
+                                      Hq, _ptr(q), _ptr(seq_ids), _ptr(positions), n,
+                                      _ptr(block_tables), block_tables.shape[1],
+                                      block_tables.shape[0], float(scale), _ptr(out),
+                                      _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(),
+                                      _ptr(status), _stream(stream)))
 
 
 def kvinj_append(cache: Cache, rope: Rope | None, layer: int, k_new, v_new, positions,

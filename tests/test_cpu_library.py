@@ -124,3 +124,28 @@ def test_strerror_and_codes():
                       ("KVINJ_ECUDA", 4), ("KVINJ_ST_BAD_CHUNK", 0x01), ("KVINJ_ST_TIMEOUT", 0x40)):
         m = re.search(rf"#define {name} (0x[0-9a-fA-F]+|\d+)", text)
         assert m and int(m.group(1), 0) == val
+
+
+def test_prefill_host_validation(lib):
+    # no GPU needed: sizes and argument checks happen before any launch
+    assert lib.kvinj_prefill_workspace_size(0, 32, 8, 128, 64) == 0
+    assert lib.kvinj_prefill_workspace_size(10, 30, 8, 128, 64) == 0  # Hq not a multiple of Hkv
+    small = lib.kvinj_prefill_workspace_size(10, 32, 8, 128, 64)
+    big = lib.kvinj_prefill_workspace_size(5000, 32, 8, 128, 64)
+    dec = lib.kvinj_decode_workspace_size(1, 32, 8, 128)
+    # the decode's workspace, then the rows' tables, context lengths and q positions
+    # (at most 1024 rows per launch), each 256-byte aligned
+    r = lambda x: (x + 255) // 256 * 256
+    assert small == r(dec) + r(10 * 64 * 4) + 2 * r(10 * 4)
+    assert big == r(dec) + r(1024 * 64 * 4) + 2 * r(1024 * 4)
+    cache = K._Cache(2, 8, 128, 16, 10, 0, 0x1000, 0x2000)
+    rr = ctypes.byref
+    # nothing to do
+    assert lib.kvinj_paged_prefill(rr(cache), None, 0, 32, None, None, None, 0, None, 4, 1, 0.0,
+                                   None, None, 0, None, None) == K.KVINJ_OK
+    # missing arrays, a workspace too small
+    assert lib.kvinj_paged_prefill(rr(cache), None, 0, 32, None, 16, 16, 3, 16, 4, 1, 0.0, 16, 16,
+                                   1 << 20, None, None) == K.KVINJ_EINVAL
+    need = lib.kvinj_prefill_workspace_size(3, 32, 8, 128, 4)
+    assert lib.kvinj_paged_prefill(rr(cache), None, 0, 32, 16, 16, 16, 3, 16, 4, 1, 0.0, 16, 16,
+                                   need - 1, None, None) == K.KVINJ_EWORKSPACE

@@ -680,6 +680,69 @@ def test_decode_window_fused_append_and_refusals():
 
 
 # ---------------------------------------------------------------------------
+# paged prefill of query tokens
+# ---------------------------------------------------------------------------
+def _prefill_case(D, G, dt, mem, nq, Hkv, seed):
+    # requests of mem[r] memory tokens then nq[r] query tokens, all already in the cache;
+    # the query tokens of the requests interleaved in the token list
+    ctx = [m + n for m, n in zip(mem, nq)]
+    kc, vc, _, bt = _decode_case(D, G, dt, ctx, Hkv=Hkv, L=2, seed=seed)
+    toks = [(r, mem[r] + i) for i in range(max(nq)) for r in range(len(mem)) if i < nq[r]]
+    seq = np.array([t[0] for t in toks], np.int32)
+    pos = np.array([t[1] for t in toks], np.int32)
+    q = gen_bits(seed + 9, (len(toks), Hkv * G, D), dt)
+    return kc, vc, bt, seq, pos, q
+
+
+def _run_prefill(kc, vc, bt, seq, pos, q, dt, theta, rope_max, status=None):
+    tdt = torch_dtype(dt)
+    D = kc.shape[-1]
+    cache = K.Cache(from_bits(kc, tdt), from_bits(vc, tdt))
+    rope = K.make_rope(theta, D, rope_max)
+    n, Hq, _ = q.shape
+    ws = K.make_prefill_workspace(n, Hq, kc.shape[2], D, bt.shape[1])
+    out = torch.full((n, Hq, D), float("nan"), dtype=tdt, device="cuda")
+    K.kvinj_paged_prefill(cache, rope, 1, from_bits(q, tdt), i32(seq), i32(pos), i32(bt), out, ws,
+                          status=status)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("D,G,Hkv", [(128, 4, 8), (128, 8, 8), (128, 1, 16), (64, 2, 4)])
+def test_paged_prefill_matches_oracle(D, G, Hkv):
+    dt, theta = W.BF16, 5e5
+    mem, nq = [40, 300, 7], [5, 17, 9]
+    kc, vc, bt, seq, pos, q = _prefill_case(D, G, dt, mem, nq, Hkv, seed=80 + G)
+    status = status_tensor()
+    got = _run_prefill(kc, vc, bt, seq, pos, q, dt, theta, 400, status=status)
+    assert status.item() == 0
+    want, st = oracle.paged_prefill(kc, vc, 1, q, seq, pos, bt, theta, dt)
+    assert st == 0
+    assert_decode_close(got, want, f"prefill D{D} G{G} Hkv{Hkv}")
+
+
+def test_paged_prefill_more_tokens_than_a_launch_and_bad_tokens():
+    # 1300 query tokens: two launches of rows; a token with a request id outside the batch
+    # or a position past the table gives a zero row and a status bit, its neighbours are
+    # unaffected
+    D, G, dt, Hkv, theta = 128, 4, W.BF16, 8, 5e5
+    mem, nq = [20, 3], [700, 600]
+    kc, vc, bt, seq, pos, q = _prefill_case(D, G, dt, mem, nq, Hkv, seed=91)
+    seq, pos = seq.copy(), pos.copy()
+    seq[5] = 7
+    pos[9] = 10 ** 6
+    status = status_tensor()
+    got = _run_prefill(kc, vc, bt, seq, pos, q, dt, theta, 1000, status=status)
+    assert status.item() & K.ST_BAD_SEQ and status.item() & K.ST_BAD_POS
+    assert not got[5].any() and not got[9].any()
+    keep = np.setdiff1d(np.arange(seq.size), [5, 9])
+    want, st = oracle.paged_prefill(kc, vc, 1, q[keep], seq[keep], pos[keep], bt, theta, dt,
+                                    n_threads=16)
+    assert st == 0
+    assert_decode_close(got[keep], want, "prefill over two launches")
+
+
+# ---------------------------------------------------------------------------
 # append + decode in one call
 # ---------------------------------------------------------------------------
 def _fused_case(D, G, dt, ctx, Hkv, seed, rotate=True):
