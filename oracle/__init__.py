@@ -1,7 +1,8 @@
 """fp64 CPU oracle for the paged KV-injection path -- TEST INFRASTRUCTURE.
 
 A plain, slow statement of what the path computes (RoPE, slot mapping,
-inject, append, block copies, paged decode attention, paged prefill of query tokens), written in C in ``kvinj_oracle.c``
+inject, append, block copies, paged decode attention, paged prefill of query tokens, int8
+rows and decode over them), written in C in ``kvinj_oracle.c``
 and wrapped here with ctypes over numpy arrays. It shares no code with the
 CUDA library in ``paged_kv_cache_inject_gb300``, and neither imports the
 other. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg
@@ -82,6 +83,11 @@ def _load():
                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, i64,
                                             f64, P, ctypes.c_int, ctypes.c_int, f64, P,
                                             ctypes.c_int]),
+                "orc_quantize_rows_i8": (None, [P, i64, ctypes.c_int, ctypes.c_int, P, P]),
+                "orc_paged_decode_i8": (i32, [P, P, P, P, ctypes.c_int, ctypes.c_int, i64,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
+                                              ctypes.c_int, P, ctypes.c_int, f64, P, ctypes.c_int,
+                                              P, ctypes.c_int, f64, P]),
                 "orc_has_openmp": (ctypes.c_int, []),
             }
             for name, (res, args) in sig.items():
@@ -240,6 +246,34 @@ def attention_bits(q_bits, q_pos, theta, K_bits, V_bits, dtype, scale=0.0, rotat
     _load().orc_attention_bits(_p(qb), int(rotate_q), float(q_pos), float(theta), _p(Kb),
                                _p(Vb), n, D, dtype, float(scale), _p(out))
     return out
+
+
+def quantize_rows_i8(bits, dtype: int):
+    """int8 codes and fp32 scales of 16-bit rows [..., D]: one scale per row."""
+    b = _c(bits, np.uint16)
+    D = b.shape[-1]
+    q = np.empty(b.shape, np.int8)
+    s = np.empty(b.shape[:-1], np.float32)
+    _load().orc_quantize_rows_i8(_p(b), b.size // D, D, dtype, _p(q), _p(s))
+    return q, s
+
+
+def paged_decode_i8(kq, ks, vq, vs, layer, q_bits, q_pos, block_tables, context_lens, theta,
+                    q_dtype, scale=0.0, rotate_q=True):
+    """paged_decode over an int8 cache (codes [L][NB][Hkv][B][D], scales [L][NB][Hkv][B])."""
+    L, NB, Hkv, B, D = kq.shape
+    kq, vq = _c(kq, np.int8), _c(vq, np.int8)
+    ks, vs = _c(ks, np.float32), _c(vs, np.float32)
+    q = _c(q_bits, np.uint16)
+    batch, Hq, _ = q.shape
+    qp = _c(q_pos, np.int32)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    out = np.empty((batch, Hq, D), np.float64)
+    st = _load().orc_paged_decode_i8(_p(kq), _p(ks), _p(vq), _p(vs), Hkv, D, NB, B, layer, Hq,
+                                     _p(q), q_dtype, _p(qp), int(rotate_q), float(theta), _p(bt),
+                                     bt.shape[1], _p(cl), batch, float(scale), _p(out))
+    return out, int(st)
 
 
 def paged_prefill(k_cache, v_cache, layer, q_bits, seq_ids, positions, block_tables, theta,

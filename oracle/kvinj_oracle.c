@@ -424,6 +424,79 @@ int32_t orc_paged_prefill(const uint16_t *k_cache, const uint16_t *v_cache, int 
   return st;
 }
 
+/* ------------------------------------------------------------------ */
+/* int8 KV cache [KM "KV cache quantization": int8 halves the cache's  */
+/* bytes]. The page fixes no scheme; the reading taken: every stored    */
+/* row (token, kv head) is quantized symmetrically on its own, scale    */
+/* s = max|x| / 127 (kept as fp32), code q = x / s rounded to nearest   */
+/* even and clamped to [-127, 127]; a zero row has s = 0. The value     */
+/* read back is q * s.                                                  */
+/* ------------------------------------------------------------------ */
+void orc_quantize_rows_i8(const uint16_t *in, int64_t n, int D, int dtype, int8_t *q,
+                          float *scale) {
+  const fmt16 *f = fmt_of(dtype);
+  for (int64_t r = 0; r < n; ++r) {
+    double amax = 0.0;
+    for (int d = 0; d < D; ++d) {
+      double x = fabs(dec16(in[r * D + d], f));
+      if (x > amax) amax = x;
+    }
+    float s = (float)(amax / 127.0);
+    scale[r] = s;
+    for (int d = 0; d < D; ++d) {
+      double v = s > 0.0f ? nearbyint(dec16(in[r * D + d], f) / (double)s) : 0.0;
+      if (v > 127.0) v = 127.0;
+      if (v < -127.0) v = -127.0;
+      q[r * D + d] = (int8_t)v;
+    }
+  }
+}
+
+/* paged decode over an int8 cache: as orc_paged_decode, each key and   */
+/* value row read back as code * its row's scale. Scales are laid out   */
+/* like the rows: [L][num_blocks][Hkv][B].                              */
+int32_t orc_paged_decode_i8(const int8_t *kq, const float *ks, const int8_t *vq, const float *vs,
+                            int Hkv, int D, int64_t num_blocks, int B, int layer, int Hq,
+                            const uint16_t *q, int q_dtype, const int32_t *q_pos, int rotate_q,
+                            double theta, const int32_t *block_tables, int max_blocks,
+                            const int32_t *context_lens, int batch, double scale, double *out) {
+  int32_t st = 0;
+  int G = Hq / Hkv;
+  const fmt16 *f = fmt_of(q_dtype);
+  if (scale <= 0.0) scale = 1.0 / sqrt((double)D);
+  for (int64_t rq = 0; rq < (int64_t)batch * Hq; ++rq) {
+    int r = (int)(rq / Hq), qh = (int)(rq % Hq), kvh = qh / G;
+    double *o = out + rq * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    int64_t ctx = context_lens[r];
+    if (ctx <= 0 || ctx > (int64_t)max_blocks * B) { st |= ORC_ST_CTX; continue; }
+    double *K = (double *)malloc(sizeof(double) * (size_t)ctx * D);
+    double *V = (double *)malloc(sizeof(double) * (size_t)ctx * D);
+    int bad = 0;
+    for (int64_t j = 0; j < ctx; ++j) {
+      int32_t b8 = block_tables[(int64_t)r * max_blocks + j / B];
+      if (b8 < 0 || b8 >= num_blocks) { bad = 1; break; }
+      int64_t e = cache_row(layer, (int64_t)b8 * B + j % B, kvh, num_blocks, Hkv, B, D);
+      for (int d = 0; d < D; ++d) {
+        K[j * D + d] = (double)kq[e + d] * (double)ks[e / D];
+        V[j * D + d] = (double)vq[e + d] * (double)vs[e / D];
+      }
+    }
+    if (bad) {
+      st |= ORC_ST_BLOCK;
+    } else {
+      double q0[1024], qr[1024];
+      for (int d = 0; d < D; ++d) q0[d] = dec16(q[rq * D + d], f);
+      if (rotate_q) orc_rope(q0, D, (double)q_pos[r], theta, qr);
+      else memcpy(qr, q0, sizeof(double) * D);
+      orc_attention(qr, K, V, ctx, D, scale, o);
+    }
+    free(K);
+    free(V);
+  }
+  return st;
+}
+
 int orc_has_openmp(void) {
 #ifdef _OPENMP
   return 1;

@@ -46,6 +46,11 @@ MUTANTS = [
     ("prefill_excludes_itself", "    int64_t ctx = (int64_t)pos[i] + 1;\n    if (r < 0",
      "    int64_t ctx = (int64_t)pos[i];\n    if (r < 0"),
     ("prefill_first_request_table", "    int r = seq[i];\n", "    int r = 0;\n"),
+    ("i8_scale_128", "float s = (float)(amax / 127.0);", "float s = (float)(amax / 128.0);"),
+    ("i8_round_floor", "double v = s > 0.0f ? nearbyint(dec16(in[r * D + d], f) / (double)s) : 0.0;",
+     "double v = s > 0.0f ? floor(dec16(in[r * D + d], f) / (double)s) : 0.0;"),
+    ("i8_value_takes_key_scale", "V[j * D + d] = (double)vq[e + d] * (double)vs[e / D];",
+     "V[j * D + d] = (double)vq[e + d] * (double)ks[e / D];"),
     ("copy_blocks_k_only", "            v_cache[to + d] = v_cache[from + d];\n", ""),
 ]
 

@@ -470,6 +470,50 @@ def test_paged_prefill_is_causal_attention_over_memory_and_query():
     assert st == 32
 
 
+def test_int8_rows_round_within_half_a_step():
+    # int8 KV ("KV Cache Management", KV cache quantization): each row read back within half
+    # a quantization step of its value, its largest magnitude on the extreme code, a zero row
+    # all zeros; scaling a row by a power of two scales its step and keeps its codes
+    rng = np.random.default_rng(37)
+    x = rng.standard_normal((60, 64)) * np.exp2(rng.integers(-12, 12, (60, 1)))
+    x[7] = 0.0
+    bits = oracle.encode(x, BF16)
+    xd = oracle.decode(bits, BF16)
+    q, s = oracle.quantize_rows_i8(bits, BF16)
+    back = q.astype(np.float64) * s[:, None].astype(np.float64)
+    assert (np.abs(back - xd) <= s[:, None].astype(np.float64) * (0.5 + 1e-6)).all()
+    nz = np.arange(60) != 7
+    assert (np.abs(q[nz].astype(int)).max(axis=1) == 127).all()
+    assert s[7] == 0 and not q[7].any()
+    q2, s2 = oracle.quantize_rows_i8(oracle.encode(xd * 8.0, BF16), BF16)
+    assert np.array_equal(q2, q) and np.array_equal(s2, s * np.float32(8.0))
+
+
+def test_int8_decode_equals_16bit_decode_on_exact_codes():
+    # rows whose values are codes times a power-of-two step (each row reaching +-127) are
+    # exactly representable in bf16 and quantize back to the same codes: decoding the int8
+    # cache must then give the 16-bit decode's outputs bit for bit
+    rng = np.random.default_rng(41)
+    L, NB, Hkv, B, D, G, theta = 1, 9, 2, 16, 64, 3, 5e5
+    codes = rng.integers(-127, 128, (2, L, NB, Hkv, B, D))
+    codes[..., 0] = np.where(rng.random(codes.shape[:-1]) < 0.5, 127, -127)
+    step = np.exp2(rng.integers(-9, -3, (2, L, NB, Hkv, B, 1))).astype(np.float64)
+    kc = oracle.encode(codes[0] * step[0], BF16)
+    vc = oracle.encode(codes[1] * step[1], BF16)
+    kq, ks = oracle.quantize_rows_i8(kc, BF16)
+    vq, vs = oracle.quantize_rows_i8(vc, BF16)
+    assert np.array_equal(kq, codes[0]) and np.array_equal(ks, step[0][..., 0].astype(np.float32))
+    assert np.array_equal(vq, codes[1])
+    ctx = np.array([60, 33], np.int32)  # 4 and 3 pages of 16
+    bt = rng.permutation(NB)[:8].astype(np.int32).reshape(2, 4)
+    bt[1, 3] = -1
+    q = oracle.encode(rng.standard_normal((2, Hkv * G, D)), BF16)
+    want, st = oracle.paged_decode(kc, vc, 0, q, ctx - 1, bt, ctx, theta, BF16)
+    assert st == 0
+    got, st = oracle.paged_decode_i8(kq, ks, vq, vs, 0, q, ctx - 1, bt, ctx, theta, BF16)
+    assert st == 0 and np.array_equal(got, want)
+
+
 def test_gqa_groups_are_consecutive_query_heads():
     # "groups of four share one key and value head" ("LLM Inference: KV Caching");
     # reading: query heads g*G .. g*G+G-1 use kv head g
