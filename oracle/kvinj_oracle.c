@@ -134,10 +134,11 @@ void orc_rope(const double *x, int D, double pos, double theta, double *y) {
 static void rope_round_row(const uint16_t *in, int D, double pos, double theta, int dtype,
                            uint16_t *out) {
   const fmt16 *f = fmt_of(dtype);
-  double x[1024], y[1024];
+  double *x = (double *)malloc(sizeof(double) * 2 * (size_t)D), *y = x + D;
   for (int d = 0; d < D; ++d) x[d] = dec16(in[d], f);
   orc_rope(x, D, pos, theta, y);
   for (int d = 0; d < D; ++d) out[d] = enc16(y[d], f);
+  free(x);
 }
 
 void orc_rope_round_rows(const uint16_t *in, int64_t n, int D, const int32_t *positions,
@@ -316,7 +317,7 @@ void orc_attention_bits(const uint16_t *q_bits, int rotate_q, double q_pos, doub
                         const uint16_t *K_bits, const uint16_t *V_bits, int64_t n, int D,
                         int dtype, double scale, double *out) {
   const fmt16 *f = fmt_of(dtype);
-  double q0[1024], q[1024];
+  double *q0 = (double *)malloc(sizeof(double) * 2 * (size_t)D), *q = q0 + D;
   for (int d = 0; d < D; ++d) q0[d] = dec16(q_bits[d], f);
   if (rotate_q) orc_rope(q0, D, q_pos, theta, q);
   else memcpy(q, q0, sizeof(double) * D);
@@ -329,6 +330,7 @@ void orc_attention_bits(const uint16_t *q_bits, int rotate_q, double q_pos, doub
   orc_attention(q, K, V, n, D, scale, out);
   free(K);
   free(V);
+  free(q0);
 }
 
 /* ------------------------------------------------------------------ */
@@ -485,11 +487,12 @@ int32_t orc_paged_decode_i8(const int8_t *kq, const float *ks, const int8_t *vq,
     if (bad) {
       st |= ORC_ST_BLOCK;
     } else {
-      double q0[1024], qr[1024];
+      double *q0 = (double *)malloc(sizeof(double) * 2 * (size_t)D), *qr = q0 + D;
       for (int d = 0; d < D; ++d) q0[d] = dec16(q[rq * D + d], f);
       if (rotate_q) orc_rope(q0, D, (double)q_pos[r], theta, qr);
       else memcpy(qr, q0, sizeof(double) * D);
       orc_attention(qr, K, V, ctx, D, scale, o);
+      free(q0);
     }
     free(K);
     free(V);
