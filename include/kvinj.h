@@ -247,14 +247,30 @@ int kvinj_paged_prefill(const kvinj_cache *cache, const kvinj_rope *rope, int32_
  * are read, so table entries of pages wholly before the window may hold
  * anything. Runs the tcgen05 kernel: D = 128, Hkv a multiple of 8, G in
  * {1, 2, 4, 8}, else KVINJ_EUNSUPPORTED; window < 0 or only one of k_new,
- * v_new: KVINJ_EINVAL. */
+ * v_new: KVINJ_EINVAL. `flags`: KVINJ_DECODE_* bits, as kvinj_paged_decode_ex. */
 int kvinj_paged_decode_window(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
                               int32_t num_q_heads, const void *q, const void *k_new,
                               const void *v_new, const int32_t *q_pos,
                               const int32_t *block_tables, int32_t max_blocks,
                               const int32_t *context_lens, int32_t batch, int32_t window,
                               float scale, void *out, void *workspace, size_t ws_bytes,
-                              int32_t *dev_status, kvinj_stream_t stream);
+                              int32_t *dev_status, kvinj_stream_t stream, int32_t flags);
+
+/* Flags of the decode calls that take them (bit set).
+ *
+ * KVINJ_DECODE_KV_READY: the cache pages of `layer`, the block tables, the
+ * context lengths and the q positions this call reads were all written by work
+ * enqueued on the stream before the previous decode call on that stream, and
+ * that previous call appended into another layer (or appended nothing). The
+ * split-K pass may then start reading them -- its prologue and its first
+ * stages of K/V pages -- while the kernels ahead of it on the stream are still
+ * running (it is launched as their programmatic dependent); it waits for them
+ * before it reads q, k_new, v_new or the RoPE table and before it writes
+ * anything. Typical use: every layer's call of a decode step but the first
+ * after the inject, when q comes from the kernel just before. Applies to the
+ * tcgen05 kernel (ignored by the others); without it every read waits. A
+ * call that sets it when the condition does not hold may read stale pages. */
+#define KVINJ_DECODE_KV_READY 1
 
 /* Same as kvinj_paged_decode with an explicit kernel choice (G = Hq/Hkv):
  * variant 0 = automatic (3 where it applies, else 2 for G >= 4, else 1),
@@ -264,13 +280,14 @@ int kvinj_paged_decode_window(const kvinj_cache *cache, const kvinj_rope *rope, 
  *     of 8, G in {1, 2, 4, 8}).
  * KVINJ_EUNSUPPORTED when the chosen variant does not cover the shape.
  * `ctas` > 0 overrides the grid size (1 .. 2 x the SM count, the workspace
- * slots); 0 = one CTA per SM. */
+ * slots); 0 = one CTA per SM. `flags`: KVINJ_DECODE_* bits (0: none; an
+ * unknown bit is KVINJ_EINVAL). */
 int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
                           int32_t num_q_heads, const void *q, const int32_t *q_pos,
                           const int32_t *block_tables, int32_t max_blocks,
                           const int32_t *context_lens, int32_t batch, float scale, void *out,
                           void *workspace, size_t ws_bytes, int32_t *dev_status,
-                          kvinj_stream_t stream, int32_t variant, int32_t ctas);
+                          kvinj_stream_t stream, int32_t variant, int32_t ctas, int32_t flags);
 
 /* Append, then decode ([KC] "The fix": each step appends the new token's K
  * and V, then attends over the whole cache). For request r < batch the token
@@ -299,23 +316,32 @@ int kvinj_append_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rop
                                  const int32_t *context_lens, int32_t batch, float scale,
                                  void *out, void *workspace, size_t ws_bytes,
                                  int32_t *dev_status, kvinj_stream_t stream, int32_t variant,
-                                 int32_t ctas);
+                                 int32_t ctas, int32_t flags);
 
 /* Paged decode without a caller-provided workspace (no counterpart in the
  * pages; an addition of this library). For callers that cannot allocate
  * device memory where they run -- an engine hook or plugin that must not call
  * cudaMalloc (it can implicitly synchronize the device), a process whose
  * memory is already handed out, a path that must not fail on memory
- * pressure mid-request. Same arguments and results as kvinj_paged_decode;
- * the scratch is a fixed device array of KVINJ_STATIC_SCRATCH_BYTES that
- * every GPU loading this library holds until exit. Nothing is allocated or
- * freed. Returns KVINJ_EWORKSPACE when this shape needs more scratch than
- * that (kvinj_decode_workspace_size() > KVINJ_STATIC_SCRATCH_BYTES; enough
- * for D = 128 with up to 64 query heads per head group on a 152-SM GPU).
- * The first call on a device looks up the array's address (make it before
- * any stream capture). All calls on a device share the array and leave their
- * contents in it; nothing in it needs to start at zero, but calls whose
- * kernels overlap on the GPU race on it. */
+ * pressure mid-request. Same arguments and results as kvinj_paged_decode
+ * (bit for bit: the same kernels on the same inputs); the scratch is a fixed
+ * device array of KVINJ_STATIC_SCRATCH_BYTES that every GPU loading this
+ * library holds until exit. Nothing is allocated or freed.
+ * Size limit: a shape is accepted when kvinj_decode_workspace_size() for it
+ * on the current device is at most KVINJ_STATIC_SCRATCH_BYTES, i.e. when
+ *   header + 2 * (2 * SMs) * HG * G * (D + 2) * 4 <= 24 MiB
+ * with HG = the largest power of two <= 8 dividing Hkv, G = Hq / Hkv and SMs
+ * the device's multiprocessor count (the header is 2 * SMs * 32 bytes rounded
+ * up to 256). On a 152-SM GPU that admits G = 8 at D = 128 with HG = 8 (about
+ * 19.3 MiB); the requirement grows with the SM count, so call
+ * kvinj_decode_workspace_size() to test a shape on the device at hand; larger
+ * shapes return KVINJ_EWORKSPACE.
+ * Every call looks up the array's device address in the current context (it
+ * is not cached, so a device reset cannot leave a stale address behind); the
+ * first call on a device may load the library's device code there, so make
+ * it before any stream capture. All calls on a device share the array and
+ * leave their contents in it; nothing in it needs to start at zero, but calls
+ * whose kernels overlap on the GPU race on it. */
 #define KVINJ_STATIC_SCRATCH_BYTES (24u << 20)
 int kvinj_paged_decode_static(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
                               int32_t num_q_heads, const void *q, const int32_t *q_pos,

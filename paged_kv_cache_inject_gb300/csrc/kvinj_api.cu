@@ -285,7 +285,7 @@ int decode_call(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
                 const int32_t *q_pos, const int32_t *block_tables, int32_t max_blocks,
                 const int32_t *context_lens, int32_t batch, float scale, void *out,
                 void *workspace, size_t ws_bytes, int32_t *dev_status, kvinj_stream_t stream,
-                int32_t variant, int32_t ctas, int32_t window = 0) {
+                int32_t variant, int32_t ctas, int32_t window = 0, int32_t flags = 0) {
   int rc = check_cache(cache, true);
   if (rc) return rc;
   const int D = cache->head_dim, Hkv = cache->num_kv_heads;
@@ -301,6 +301,7 @@ int decode_call(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
     return KVINJ_EINVAL;
   if (!aligned16(q) || !aligned16(out)) return KVINJ_EINVAL;
   if (variant < 0 || variant > 3) return KVINJ_EINVAL;
+  if (flags & ~KVINJ_DECODE_KV_READY) return KVINJ_EINVAL;
   const bool g_pow2_8 = G == 1 || G == 2 || G == 4 || G == 8;
   const bool umma_ok = D == 128 && decode_head_group(Hkv) == 8 && g_pow2_8;
   // automatic: tcgen05 wherever it applies (at G = 8 with units of two blocks of 4 kv
@@ -374,6 +375,9 @@ int decode_call(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
   a.num_blocks = cache->num_blocks;
   a.ctas = ctas;
   a.window = window;
+  // early reads of pages, tables and lengths: the tcgen05 kernel only (the others wait
+  // for the kernel ahead before anything)
+  a.early = (flags & KVINJ_DECODE_KV_READY) && variant == 3 ? 1 : 0;
   const double sc = scale > 0.f ? (double)scale : 1.0 / sqrt((double)D);
   a.scale_log2 = (float)(sc * 1.4426950408889634);
   return cuda_rc(launch_decode(a, tmK, tmV, D, G, HG, cache->dtype, variant, ctas,
@@ -387,10 +391,10 @@ int kvinj_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope, int3
                           const int32_t *block_tables, int32_t max_blocks,
                           const int32_t *context_lens, int32_t batch, float scale, void *out,
                           void *workspace, size_t ws_bytes, int32_t *dev_status,
-                          kvinj_stream_t stream, int32_t variant, int32_t ctas) {
+                          kvinj_stream_t stream, int32_t variant, int32_t ctas, int32_t flags) {
   return decode_call(cache, rope, layer, num_q_heads, q, nullptr, nullptr, q_pos, block_tables,
                      max_blocks, context_lens, batch, scale, out, workspace, ws_bytes,
-                     dev_status, stream, variant, ctas);
+                     dev_status, stream, variant, ctas, 0, flags);
 }
 
 int kvinj_append_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rope,
@@ -400,11 +404,11 @@ int kvinj_append_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rop
                                  const int32_t *context_lens, int32_t batch, float scale,
                                  void *out, void *workspace, size_t ws_bytes,
                                  int32_t *dev_status, kvinj_stream_t stream, int32_t variant,
-                                 int32_t ctas) {
+                                 int32_t ctas, int32_t flags) {
   if (!k_new || !v_new) return KVINJ_EINVAL;
   return decode_call(cache, rope, layer, num_q_heads, q, k_new, v_new, q_pos, block_tables,
                      max_blocks, context_lens, batch, scale, out, workspace, ws_bytes,
-                     dev_status, stream, variant, ctas);
+                     dev_status, stream, variant, ctas, 0, flags);
 }
 
 // query tokens per decode launch of a prefill
@@ -466,11 +470,11 @@ int kvinj_paged_decode_window(const kvinj_cache *cache, const kvinj_rope *rope, 
                               const int32_t *block_tables, int32_t max_blocks,
                               const int32_t *context_lens, int32_t batch, int32_t window,
                               float scale, void *out, void *workspace, size_t ws_bytes,
-                              int32_t *dev_status, kvinj_stream_t stream) {
+                              int32_t *dev_status, kvinj_stream_t stream, int32_t flags) {
   if ((k_new == nullptr) != (v_new == nullptr)) return KVINJ_EINVAL;
   return decode_call(cache, rope, layer, num_q_heads, q, k_new, v_new, q_pos, block_tables,
                      max_blocks, context_lens, batch, scale, out, workspace, ws_bytes,
-                     dev_status, stream, 0, 0, window);
+                     dev_status, stream, 0, 0, window, flags);
 }
 
 int kvinj_append_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
@@ -482,7 +486,7 @@ int kvinj_append_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, 
                               kvinj_stream_t stream) {
   return kvinj_append_paged_decode_ex(cache, rope, layer, num_q_heads, q, k_new, v_new, q_pos,
                                       block_tables, max_blocks, context_lens, batch, scale, out,
-                                      workspace, ws_bytes, dev_status, stream, 0, 0);
+                                      workspace, ws_bytes, dev_status, stream, 0, 0, 0);
 }
 
 int kvinj_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
@@ -493,7 +497,7 @@ int kvinj_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t
                        kvinj_stream_t stream) {
   return kvinj_paged_decode_ex(cache, rope, layer, num_q_heads, q, q_pos, block_tables,
                                max_blocks, context_lens, batch, scale, out, workspace, ws_bytes,
-                               dev_status, stream, 0, 0);
+                               dev_status, stream, 0, 0, 0);
 }
 
 int64_t kvinj_kv_bytes(int32_t layers, int32_t heads, int32_t head_dim, int64_t tokens,

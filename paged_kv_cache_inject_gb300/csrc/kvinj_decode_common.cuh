@@ -186,16 +186,47 @@ __device__ __forceinline__ int context_units(const DecodeArgs &a, int c) {
   return u > 0 ? u - window_lo(a, c) / (BLK * BPU) : 0;  // from the first attended token's
 }
 
-// Units per request -> prefix sums pre[0..batch], this CTA's range, barrier
-// set-up. CTA 0 also zeroes the output of requests whose context length is
-// invalid. Returns false when this CTA has no units.
-template <class Lay, int NT>
-__device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) {
-  // launched as a programmatic dependent: every input may come from the
-  // kernel before this one, so nothing is read before it has completed
+// The wait for the kernel ahead of this one on the stream (launched as its
+// programmatic dependent), then the release of this kernel's own dependent
+// (the combine pass, which waits for this grid's completion). Every thread
+// that reads an input another kernel may produce, or writes anything, runs
+// this first. Releasing only after the wait keeps the chain that early reads
+// rely on: once a kernel after this one starts, everything enqueued before
+// this kernel has completed.
+__device__ __forceinline__ void decode_dependency_wait() {
   griddep_wait();
-  // the combine pass may launch now: it waits for this grid's completion
   griddep_launch_dependents();
+}
+
+// CTA 0, after the dependency wait: a zero output and KVINJ_ST_BAD_CTX for
+// every request whose context length is invalid (pre[r + 1] == pre[r]);
+// threads t0, t0 + nt, ... of the CTA take the requests in turn.
+template <int D>
+__device__ void zero_invalid_outputs(const DecodeArgs &a, const int *pre, int t0, int nt) {
+  if (blockIdx.x != 0) return;
+  for (int r = t0; r < a.batch; r += nt) {
+    if (pre[r + 1] != pre[r]) continue;
+    uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t)r * a.Hq * D);
+    for (int i = 0; i < a.Hq * D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+    report(a.status, KVINJ_ST_BAD_CTX);
+  }
+}
+
+// Units per request -> prefix sums pre[0..batch], this CTA's range, barrier
+// set-up. Returns false when this CTA has no units.
+//
+// EARLY = false (every input may come from the kernel before this one): all
+// threads wait for that kernel first, and CTA 0 zeroes the output of requests
+// whose context length is invalid. EARLY = true (a call with
+// KVINJ_DECODE_KV_READY): the context lengths, q positions and block tables
+// were written before the previous decode call on the stream, so they are read
+// here before the wait; the caller then runs decode_dependency_wait() in each
+// thread before any other read or write (the producer after it has issued the
+// first stages) and zero_invalid_outputs() from CTA 0. The two are separate
+// instantiations: the waiting one carries none of the early code.
+template <class Lay, int NT, bool EARLY = false>
+__device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) {
+  if constexpr (!EARLY) decode_dependency_wait();
   int *pre = reinterpret_cast<int *>(sm + Lay::off_pre);
   int *flags = reinterpret_cast<int *>(sm + Lay::off_flags);
   const int tid = threadIdx.x;
@@ -203,7 +234,7 @@ __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) 
   unit_prefix<NT>(a, pre, flags + 8, [&](int r, int c) {
     if constexpr (Lay::QPOS_SM) pre[a.batch + 1 + r] = a.q_pos ? __ldg(a.q_pos + r) : -1;
     const int v = context_units<Lay::BPU>(a, c) * ngrp;
-    if (v == 0 && blockIdx.x == 0) {
+    if (!EARLY && v == 0 && blockIdx.x == 0) {
       uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t)r * a.Hq * Lay::D);
       for (int i = 0; i < a.Hq * Lay::D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
       report(a.status, KVINJ_ST_BAD_CTX);
@@ -242,8 +273,10 @@ __device__ bool decode_prologue(const DecodeArgs &a, uint8_t *sm, CtaRange &rg) 
 
 // Producer warp: stream this CTA's units into the stage ring. Block-table
 // entries are fetched one per lane, a batch of 32 ahead of their use; lane 0
-// issues the copies (NBOX boxes of K and NBOX boxes of V per unit).
-template <class Lay>
+// issues the copies (NBOX boxes of K and NBOX boxes of V per unit). With
+// EARLY, the first stages are issued before the dependency wait (see
+// decode_prologue).
+template <class Lay, bool EARLY = false>
 __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
                                 const CUtensorMap &tmV, uint8_t *sm, const CtaRange &rg,
                                 int lane) {
@@ -307,18 +340,32 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
   int pieces = 0, cur_piece = -1;
   int kiss = 0, viss = 0;  // (lane 0) units whose K (V) copies were issued
   bool aborted = false;
+  // early: the first stages are issued before the dependency wait, up to the first
+  // unit that holds a fused append (its rows are written after the wait); status
+  // bits found before the wait are reported after it
+  bool waited = !EARLY;
+  int pending = 0;
   for (int g0 = 0; g0 < n && !aborted; g0 += 32) {
     // valid bits: block 0 (and, with two blocks per unit, block 1) in the cache
     const int ok0 = (blk >= 0 && blk < a.num_blocks) ? 1 : 0;
     const int ok1 = (Lay::BPU == 2 && blk2 >= 0 && blk2 < a.num_blocks) ? 2 : 0;
-    if (g0 + lane < n && (!ok0 || (blk2 != -2 && Lay::BPU == 2 && !ok1)))
-      report(a.status, KVINJ_ST_BAD_BLOCK);
+    if (g0 + lane < n && (!ok0 || (blk2 != -2 && Lay::BPU == 2 && !ok1))) {
+      if constexpr (EARLY) pending |= KVINJ_ST_BAD_BLOCK;
+      else report(a.status, KVINJ_ST_BAD_BLOCK);
+    }
+    if constexpr (EARLY) {
+      if (waited && pending) {
+        report(a.status, pending);
+        pending = 0;
+      }
+    }
     const int ok = ok0 | ok1;
     const int row0 = (int)((((int64_t)a.layer * a.num_blocks + (ok0 ? blk : 0)) * a.Hkv +
                             (int64_t)hg * HG) * BLK);
     const int row1 = (int)((((int64_t)a.layer * a.num_blocks + (ok1 ? blk2 : (ok0 ? blk : 0))) *
                                 a.Hkv + (int64_t)hg * HG) * BLK);
     const int qpos_ok = (qp >= 0 && qp < a.max_pos) ? qp : -1;
+    // (the kernels that stage q in the producer run without EARLY)
     if (Lay::QB && first && a.rope && qpos_ok < 0 && g0 + lane < n) report(a.status, KVINJ_ST_BAD_POS);
     const int qrow0 = rq * a.Hq + hg * HG * Lay::G;  // first q row of the head group
     int nblk, nblk2, nhg, nrq, nfirst, nqp, nap;
@@ -335,6 +382,16 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
       const int gi = g0 + i, st = gi % S;
       int go = 1;
       if (fi) ++cur_piece;
+      if constexpr (EARLY) {
+        if (!waited && (gi >= S || api)) {
+          // the stages are all issued (the next needs a consumer), or this unit holds
+          // the fused append: wait for the kernel ahead, then report what was found
+          decode_dependency_wait();
+          waited = true;
+          if (pending) report(a.status, pending);
+          pending = 0;
+        }
+      }
       if (lane == 0) {
         if constexpr (Lay::APPEND_WAIT) {
           // the piece's query warps write the appended token before its block is read
@@ -429,6 +486,13 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
     first = nfirst;
     qp = nqp;
     ap = nap;
+  }
+  if constexpr (EARLY) {
+    if (!waited) {
+      // fewer units than stages, none with an append: the wait still precedes the exit
+      decode_dependency_wait();
+      if (pending) report(a.status, pending);
+    }
   }
   if (aborted && lane == 0) {
     // let the copies already in flight land before the CTA can exit
@@ -554,10 +618,19 @@ __device__ void combine_rows(const DecodeArgs &a, const CtaRange &rg, const Piec
 // combine per layer: one CTA per segment with two rows per warp 50.5 us; one
 // warp per row over a grid of decode CTAs 42.9 us; this grid of segments: see
 // the design notes.)
+//
+// RELEASE_EARLY: the kernel after this one is released at this pass's start
+// instead of after its dependency wait. That kernel still waits for this grid's
+// completion before it reads anything this pass writes; what it gains is that
+// its CTAs may be scheduled (and a decode call with early page reads may start
+// streaming) as soon as the split-K pass's CTAs leave their SMs. Everything
+// enqueued before the split-K pass has completed by then (the split-K pass
+// released this grid only after its own dependency wait).
 constexpr int COMBINE_WARPS = 8;
-template <int D, int G, int HG, int DT, int BPU>
+template <int D, int G, int HG, int DT, int BPU, bool RELEASE_EARLY = false>
 __global__ void __launch_bounds__(COMBINE_WARPS * 32) decode_combine_kernel(DecodeArgs a) {
   extern __shared__ int comb_sm[];  // scratch[COMBINE_WARPS], pre[batch + 1]
+  if constexpr (RELEASE_EARLY) griddep_launch_dependents();
   int *pre = comb_sm + COMBINE_WARPS;
   const int ngrp = a.Hkv / HG;
   unit_prefix<COMBINE_WARPS * 32>(a, pre, comb_sm,
@@ -589,7 +662,7 @@ __global__ void __launch_bounds__(COMBINE_WARPS * 32) decode_combine_kernel(Deco
     }
   }
   griddep_wait();  // the split-K pass complete, its partial states visible
-  griddep_launch_dependents();
+  if constexpr (!RELEASE_EARLY) griddep_launch_dependents();
   if (row >= ROWS) return;
   const int rows[1] = {row};
   combine_rows<D, G, HG, DT, 1>(a, rg, pc, rows, lane);
@@ -616,11 +689,11 @@ cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, c
 }
 
 // the combine pass for a split-K grid of `ctas` CTAs
-template <int D, int G, int HG, int DT, int BPU = 1>
+template <int D, int G, int HG, int DT, int BPU = 1, bool RELEASE_EARLY = false>
 cudaError_t launch_combine(const DecodeArgs &a, int ctas, cudaStream_t s) {
   DecodeArgs c = a;
   c.ctas = ctas;
-  return launch_pdl(decode_combine_kernel<D, G, HG, DT, BPU>,
+  return launch_pdl(decode_combine_kernel<D, G, HG, DT, BPU, RELEASE_EARLY>,
                     dim3(a.batch * (a.Hkv / HG), (HG * G + COMBINE_WARPS - 1) / COMBINE_WARPS),
                     dim3(COMBINE_WARPS * 32), (size_t)(COMBINE_WARPS + a.batch + 1) * sizeof(int),
                     s, c);

@@ -58,6 +58,8 @@ struct DecodeArgs {
   int batch, Hq, Hkv, max_blocks, layer;
   int ctas;                    // split-K grid size (set for the combine pass)
   int window;                  // sliding window in tokens (0: the whole context)
+  int early;                   // context lengths, q positions, block tables and cache pages
+                               // may be read before the dependency wait (KVINJ_DECODE_KV_READY)
   int64_t num_blocks;
   float scale_log2;            // softmax scale times log2(e)
 };

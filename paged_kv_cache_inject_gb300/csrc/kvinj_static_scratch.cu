@@ -12,19 +12,21 @@
 // the array below: KVINJ_STATIC_SCRATCH_BYTES of device memory that every GPU
 // which loads this library holds until the process exits.
 //
-// Set-up: the array's device address is looked up with cudaGetSymbolAddress
-// the first time the entry point runs on a device (with that device current)
-// and cached per device; the first call on each device should therefore come
-// before any stream capture. Host code never passes the array's name itself
-// to a kernel (in host code it is only a stand-in for the device symbol).
+// Set-up: every call looks up the array's device address on the current
+// device with cudaGetSymbolAddress (a host-side lookup, no stream work) and
+// passes that address to the kernels; host code never hands the array's name
+// itself to a kernel (in host code it is only a stand-in for the device
+// symbol). The address is not cached: after a cudaDeviceReset, or when the
+// device's primary context is destroyed and recreated, the module is loaded
+// again and the array may sit elsewhere, and a cached address would point at
+// freed memory. The first call on a device loads this library's device code
+// there if nothing else has, so make it before any stream capture.
 //
 // Sharing: every call on a device uses the same array and leaves the last
 // call's contents there. Nothing in it needs to start at zero (each call
 // writes every descriptor and partial state before reading it), but two calls
 // whose kernels overlap on the GPU (different streams, no ordering between
 // them) race on the array and may corrupt each other's results.
-#include <mutex>
-
 #include "kvinj.h"
 #include "kvinj_internal.h"
 
@@ -32,21 +34,15 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_decode_scratch[KVINJ_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_lock;
-void *g_addr[kMaxDevices] = {nullptr};
-
-// device address of g_decode_scratch for the current device (looked up once)
+// device address of g_decode_scratch in the current device's context
 int scratch_address(void **out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVINJ_ECUDA;
-  std::lock_guard<std::mutex> guard(g_lock);
-  if (!g_addr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return KVINJ_ECUDA;
-    g_addr[dev] = p;
+  void *p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+  if (e != cudaSuccess || !p) {
+    if (e != cudaSuccess) cudaGetLastError();  // not sticky: clear it
+    return KVINJ_ECUDA;
   }
-  *out = g_addr[dev];
+  *out = p;
   return KVINJ_OK;
 }
 

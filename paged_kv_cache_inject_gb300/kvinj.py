@@ -23,6 +23,8 @@ KVINJ_BF16, KVINJ_FP16 = 0, 1
 KVINJ_OK, KVINJ_EINVAL, KVINJ_EUNSUPPORTED, KVINJ_EWORKSPACE, KVINJ_ECUDA = 0, 1, 2, 3, 4
 ST_BAD_CHUNK, ST_BAD_SLOT, ST_BAD_BLOCK, ST_BAD_POS = 0x01, 0x02, 0x04, 0x08
 ST_BAD_CTX, ST_BAD_SEQ, ST_TIMEOUT, ST_INTERNAL = 0x10, 0x20, 0x40, 0x80
+KVINJ_STATIC_SCRATCH_BYTES = 24 << 20  # size of the fixed scratch of kvinj_paged_decode_static
+KVINJ_DECODE_KV_READY = 1  # decode flag: pages/tables/lengths final before the previous decode call
 
 EXPORTS = [
     "kvinj_rope_table_bytes", "kvinj_rope_table_host", "kvinj_slot_mapping", "kvinj_inject",
@@ -86,18 +88,19 @@ def load(path: str = LIB_PATH):
                                                    ctypes.c_float, P, P, sz, P, P]),
             "kvinj_paged_decode_window": (ctypes.c_int, [P, P, i32, i32, P, P, P, P, P, i32, P,
                                                          i32, i32, ctypes.c_float, P, P, sz, P,
-                                                         P]),
+                                                         P, i32]),
             "kvinj_decode_workspace_size": (sz, [i32, i32, i32, i32]),
             "kvinj_decode_workspace_init": (ctypes.c_int, [P, sz, P]),
             "kvinj_paged_decode": (ctypes.c_int, [P, P, i32, i32, P, P, P, i32, P, i32,
                                                   ctypes.c_float, P, P, sz, P, P]),
             "kvinj_paged_decode_ex": (ctypes.c_int, [P, P, i32, i32, P, P, P, i32, P, i32,
-                                                     ctypes.c_float, P, P, sz, P, P, i32, i32]),
+                                                     ctypes.c_float, P, P, sz, P, P, i32, i32,
+                                                     i32]),
             "kvinj_append_paged_decode": (ctypes.c_int, [P, P, i32, i32, P, P, P, P, P, i32, P,
                                                          i32, ctypes.c_float, P, P, sz, P, P]),
             "kvinj_append_paged_decode_ex": (ctypes.c_int, [P, P, i32, i32, P, P, P, P, P, i32,
                                                             P, i32, ctypes.c_float, P, P, sz, P,
-                                                            P, i32, i32]),
+                                                            P, i32, i32, i32]),
             "kvinj_paged_decode_static": (ctypes.c_int, [P, P, i32, i32, P, P, P, i32, P, i32,
                                                          ctypes.c_float, P, P, P]),
             "kvinj_kv_bytes": (i64, [i32, i32, i32, i64, i32]),
@@ -250,9 +253,9 @@ def kvinj_copy_blocks(cache: Cache, src, dst, layer_begin: int = 0, layer_end: i
 def kvinj_paged_decode_window(cache: Cache, rope: Rope | None, layer: int, q, q_pos,
                               block_tables, context_lens, window: int, out, workspace,
                               k_new=None, v_new=None, scale: float = 0.0, status=None,
-                              stream=None):
+                              stream=None, flags: int = 0):
     """Paged decode over the last `window` tokens of each context (0: all of them), with
-    the new token's append fused when k_new and v_new are given."""
+    the new token's append fused when k_new and v_new are given; flags: KVINJ_DECODE_*."""
     batch, Hq, _ = q.shape
     _check("kvinj_paged_decode_window",
            load().kvinj_paged_decode_window(
@@ -261,7 +264,7 @@ def kvinj_paged_decode_window(cache: Cache, rope: Rope | None, layer: int, q, q_
                _ptr(v_new) if v_new is not None else None, _ptr(q_pos), _ptr(block_tables),
                block_tables.shape[1], _ptr(context_lens), batch, window, float(scale), _ptr(out),
                _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
-               _stream(stream)))
+               _stream(stream), int(flags)))
 
 
 def kvinj_prefill_workspace_size(n: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
@@ -348,7 +351,7 @@ def kvinj_paged_decode_static(cache: Cache, rope: Rope | None, layer: int, q, q_
 
 def kvinj_paged_decode_ex(cache: Cache, rope: Rope | None, layer: int, q, q_pos, block_tables,
                           context_lens, out, workspace, scale: float = 0.0, status=None,
-                          stream=None, variant: int = 0, ctas: int = 0):
+                          stream=None, variant: int = 0, ctas: int = 0, flags: int = 0):
     batch, Hq, _ = q.shape
     _check("kvinj_paged_decode_ex",
            load().kvinj_paged_decode_ex(cache.ref, rope.ref if rope is not None else None,
@@ -356,16 +359,17 @@ def kvinj_paged_decode_ex(cache: Cache, rope: Rope | None, layer: int, q, q_pos,
                                         block_tables.shape[1], _ptr(context_lens), batch,
                                         float(scale), _ptr(out), _ptr(workspace),
                                         workspace.numel() * workspace.element_size(),
-                                        _ptr(status), _stream(stream), variant, ctas))
+                                        _ptr(status), _stream(stream), variant, ctas,
+                                        int(flags)))
     return out
 
 
 def kvinj_append_paged_decode(cache: Cache, rope: Rope | None, layer: int, q, k_new, v_new,
                               q_pos, block_tables, context_lens, out, workspace,
                               scale: float = 0.0, status=None, stream=None, variant: int = 0,
-                              ctas: int = 0):
+                              ctas: int = 0, flags: int = 0):
     """Append the token at q_pos of every request (k_new, v_new [batch][Hkv][D]), then
-    decode; variant/ctas as in kvinj_paged_decode_ex (0: automatic)."""
+    decode; variant/ctas/flags as in kvinj_paged_decode_ex (0: automatic, none)."""
     batch, Hq, _ = q.shape
     _check("kvinj_append_paged_decode_ex",
            load().kvinj_append_paged_decode_ex(
@@ -373,5 +377,5 @@ def kvinj_append_paged_decode(cache: Cache, rope: Rope | None, layer: int, q, k_
                _ptr(k_new), _ptr(v_new), _ptr(q_pos), _ptr(block_tables), block_tables.shape[1],
                _ptr(context_lens), batch, float(scale), _ptr(out), _ptr(workspace),
                workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream),
-               variant, ctas))
+               variant, ctas, int(flags)))
     return out

@@ -149,3 +149,28 @@ def test_prefill_host_validation(lib):
     need = lib.kvinj_prefill_workspace_size(3, 32, 8, 128, 4)
     assert lib.kvinj_paged_prefill(rr(cache), None, 0, 32, 16, 16, 16, 3, 16, 4, 1, 0.0, 16, 16,
                                    need - 1, None, None) == K.KVINJ_EWORKSPACE
+
+
+def test_static_scratch_size_of_the_binding_is_the_headers():
+    text = open(HEADER).read()
+    m = re.search(r"#define KVINJ_STATIC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m, "KVINJ_STATIC_SCRATCH_BYTES not found in the header"
+    assert K.KVINJ_STATIC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_decode_flags_host_validation(lib):
+    # an unknown flag bit is refused on the host before anything else runs; the one
+    # defined bit is the header's
+    text = open(HEADER).read()
+    m = re.search(r"#define KVINJ_DECODE_KV_READY (\d+)", text)
+    assert m and int(m.group(1)) == K.KVINJ_DECODE_KV_READY == 1
+    cache = K._Cache(2, 8, 128, 16, 10, 0, 0x1000, 0x2000)
+    r = ctypes.byref
+    assert lib.kvinj_paged_decode_ex(r(cache), None, 0, 32, 16, 16, 16, 4, 16, 1, 0.0, 16, 16,
+                                     1 << 30, None, None, 0, 0, 2) == K.KVINJ_EINVAL
+    assert lib.kvinj_append_paged_decode_ex(r(cache), None, 0, 32, 16, 16, 16, 16, 16, 4, 16, 1,
+                                            0.0, 16, 16, 1 << 30, None, None, 0, 0,
+                                            4) == K.KVINJ_EINVAL
+    assert lib.kvinj_paged_decode_window(r(cache), None, 0, 32, 16, None, None, 16, 16, 4, 16, 1,
+                                         0, 0.0, 16, 16, 1 << 30, None, None,
+                                         -1) == K.KVINJ_EINVAL
