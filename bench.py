@@ -1,12 +1,13 @@
 """Benchmark of the paged KV-injection hot path on GB300.
 
-One step = one pass of the whole hot path over one batch of requests of the
-Llama-3-8B-shaped workload (32 layers, 32 q / 8 kv heads, d 128, bf16,
-block 16, batch 32, contexts U[512, 2048], 8 injected chunks of 64 tokens per
-request from a resident pool of 4096 pre-RoPE chunks, 1 decode step):
+One step = one pass of the whole hot path over one batch of requests. The
+default workload is the largest one that fits one GPU, Llama-3-70B-shaped
+(80 layers, 64 q / 8 kv heads, d 128, bf16, block 16, batch 8, contexts of
+8192 tokens, 64 injected chunks of 32 tokens per request from a resident
+pool of 16384 pre-RoPE chunks, 16 decode steps with per-step append):
 
     slot mapping -> inject (gather, RoPE, scatter; all layers) ->
-    per layer: append the new token's K/V, paged GQA decode attention
+    per decode step and layer: append the new token's K/V, paged GQA decode
 
 The headline `value` is the step's algorithmic HBM traffic (bytes the step
 must move at minimum: injected chunk rows read and written, appended rows,
@@ -15,7 +16,10 @@ by the step time, in GB/s; the injection rate (injected tokens/s) and the
 decode bandwidth are reported beside it. Inputs are resident in HBM when the
 timed region starts and larger than L2 (no flush needed); `e2e` repeats the
 measurement through the engine's host-buffer entry point with the per-step
-inputs copied from pinned host memory and the outputs copied back.
+inputs copied from pinned host memory and the outputs copied back. The other
+target workloads (Llama-3-8B-shaped, multi-head 70B fp16, mixed lengths) are
+measured in the same run, each step timed the same way, under
+parts.other_workloads.
 
 --impl reference times the fp64 CPU oracle on a bounded sample (layer 0 of
 the same workload) on this machine's host cores. For N > 1 (torchrun) every
@@ -38,7 +42,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged GQA decode HBM GB/s (% of ~8 TB/s); KV-injection tokens/s"
 NOMINAL_HBM_GBS = 8000.0
-DEFAULT_CONFIG = "llama3_8b_b32"
+DEFAULT_CONFIG = "llama3_70b_b8_8k"
+# the other workloads whose steps the same run measures (reported under parts.other_workloads)
+OTHER_WORKLOADS = ["llama3_8b_b32", "mha70b_b4_4k_fp16", "mixed_b64_loguniform"]
 
 
 def _peaks():
@@ -183,43 +189,54 @@ def _source_hash() -> str:
 class OracleSample:
     """Layer 0 of the workload on the host: the oracle's slot mapping, inject,
     append of the context and step tokens, and paged decode of every query
-    head of every request. Inputs are generated once (not timed)."""
+    head, for the first `requests` requests of the batch (all of them by
+    default). Inputs are generated once (not timed)."""
 
-    def __init__(self, wl, threads: int, window: int = 0):
+    def __init__(self, wl, threads: int, window: int = 0, requests: int | None = None):
         import numpy as np
 
         import oracle
         self.np, self.oracle, self.wl, self.threads, self.window = np, oracle, wl, threads, window
         cfg = wl.cfg
+        n_req = cfg.batch if requests is None else max(1, min(int(requests), cfg.batch))
+        self.n_req = n_req
         L0 = 0
         Hkv, D, c = cfg.kv_heads, cfg.head_dim, cfg.chunk_len
-        ids = np.unique(wl.chunk_ids)
+        keep = wl.chunk_req < n_req
+        ids = np.unique(wl.chunk_ids[keep])
         # pool rows of the drawn chunks for layer 0, as [n][1][2][c][Hkv][D]
         pool = np.zeros((ids.size, 1, 2, c, Hkv, D), np.uint16)
+        t = np.tile(np.repeat(np.arange(c), Hkv), ids.size)
+        h = np.tile(np.arange(Hkv), c * ids.size)
+        cid = np.repeat(ids, c * Hkv)
         for kv in (0, 1):
-            t = np.repeat(np.arange(c), Hkv)
-            h = np.tile(np.arange(Hkv), c)
-            for u, cid in enumerate(ids):
-                pool[u, 0, kv] = wl.pool_rows(np.full(t.size, cid), np.zeros(t.size, int),
-                                              np.full(t.size, kv), t, h).reshape(c, Hkv, D)
+            pool[:, 0, kv] = wl.pool_rows(cid, np.zeros(cid.size, int), np.full(cid.size, kv), t,
+                                          h).reshape(ids.size, c, Hkv, D)
         self.pool = pool
-        self.ids = np.searchsorted(ids, wl.chunk_ids).astype(np.int32)
-        self.inj_seq, self.inj_pos = wl.injected_tokens()
+        self.ids = np.searchsorted(ids, wl.chunk_ids[keep]).astype(np.int32)
+        self.start_pos = wl.start_pos[keep]
+        inj_seq, inj_pos = wl.injected_tokens()
+        tok_keep = np.repeat(keep, c)
+        self.inj_seq, self.inj_pos = inj_seq[tok_keep], inj_pos[tok_keep]
         a_seq, a_pos = wl.appended_tokens()
+        a_keep = a_seq < n_req
+        a_seq, a_pos = a_seq[a_keep], a_pos[a_keep]
         s_seq, s_pos = wl.step_tokens(0)
+        s_seq, s_pos = s_seq[:n_req], s_pos[:n_req]
         self.app = [(a_seq, a_pos, wl.ctx_rows(L0, 0, a_seq, a_pos), wl.ctx_rows(L0, 1, a_seq, a_pos)),
                     (s_seq, s_pos, wl.ctx_rows(L0, 0, s_seq, s_pos), wl.ctx_rows(L0, 1, s_seq, s_pos))]
-        self.q = wl.q_rows(0, L0)
+        self.q = wl.q_rows(0, L0)[:n_req]
         self.q_pos = s_pos
         self.ctx = s_pos + 1
+        self.block_tables = wl.block_tables[:n_req]
         row = Hkv * D * cfg.elem_bytes
-        n_inj_tok = wl.n_inj * c
+        n_inj_tok = self.inj_pos.size
         n_app = sum(x[0].size for x in self.app)
         ctx = self.ctx.astype(np.int64)
         lo = np.maximum(ctx - window, 0) if window > 0 else np.zeros_like(ctx)
         pages = -(-ctx // cfg.block_size) - lo // cfg.block_size
         self.bytes = (2 * 2 * row * n_inj_tok + 2 * 2 * row * n_app + int((ctx - lo).sum()) * 2 * row
-                      + cfg.batch * cfg.q_heads * D * 2 * 2 + int(pages.sum()) * 4)
+                      + n_req * cfg.q_heads * D * 2 * 2 + int(pages.sum()) * 4)
         self.inj_tokens = n_inj_tok
 
     def run(self):
@@ -227,14 +244,14 @@ class OracleSample:
         shape = (1, wl.num_blocks, cfg.kv_heads, cfg.block_size, cfg.head_dim)
         kc = np.zeros(shape, np.uint16)
         vc = np.zeros(shape, np.uint16)
-        slots, _ = orc.slot_mapping(wl.block_tables, self.inj_seq, self.inj_pos, cfg.block_size,
+        slots, _ = orc.slot_mapping(self.block_tables, self.inj_seq, self.inj_pos, cfg.block_size,
                                     wl.num_blocks)
-        orc.inject(self.pool, self.ids, wl.start_pos, slots, cfg.theta, cfg.dtype, kc, vc,
+        orc.inject(self.pool, self.ids, self.start_pos, slots, cfg.theta, cfg.dtype, kc, vc,
                    n_threads=self.threads)
         for seq, pos, kn, vn in self.app:
-            sl, _ = orc.slot_mapping(wl.block_tables, seq, pos, cfg.block_size, wl.num_blocks)
+            sl, _ = orc.slot_mapping(self.block_tables, seq, pos, cfg.block_size, wl.num_blocks)
             orc.append(kc, vc, 0, kn, vn, pos, sl, cfg.theta, cfg.dtype)
-        out, _ = orc.paged_decode(kc, vc, 0, self.q, self.q_pos, wl.block_tables, self.ctx,
+        out, _ = orc.paged_decode(kc, vc, 0, self.q, self.q_pos, self.block_tables, self.ctx,
                                   cfg.theta, cfg.dtype, n_threads=self.threads,
                                   window=self.window)
         return out
@@ -242,14 +259,54 @@ class OracleSample:
     @property
     def description(self):
         cfg = self.wl.cfg
-        return (f"layer 0 of 1/{cfg.layers} layers of {cfg.name}: slot mapping, inject of "
-                f"{self.inj_tokens} tokens, append of the context and step tokens, paged decode "
-                f"of {cfg.batch}x{cfg.q_heads} query heads")
+        who = (f"{cfg.batch}" if self.n_req == cfg.batch else
+               f"the first {self.n_req} of {cfg.batch}")
+        return (f"layer 0 of 1/{cfg.layers} layers of {cfg.name}, {who} requests: slot mapping, "
+                f"inject of {self.inj_tokens} tokens, append of the context and step tokens, "
+                f"paged decode of {self.n_req}x{cfg.q_heads} query heads")
+
+    def time(self, min_seconds: float):
+        """Repeat run() for at least min_seconds; (bytes per second, runs, seconds)."""
+        runs, t0 = 0, time.perf_counter()
+        while True:
+            self.run()
+            runs += 1
+            dt = time.perf_counter() - t0
+            if dt >= min_seconds:
+                return self.bytes * runs / dt, runs, dt
 
 
 def oracle_threads() -> int:
     import oracle
     return (os.cpu_count() or 1) if oracle.has_openmp() else 1
+
+
+def single_thread_requests(cfg) -> int:
+    """Requests of the single-threaded oracle sample: about a quarter of the
+    batch's context tokens (at least one request), so that one run stays near
+    ten seconds on one host core."""
+    import numpy as np
+
+    import workload as W
+    wl = W.make_workload(cfg)
+    ctx = np.cumsum(wl.context_lens.astype(np.int64))
+    return int(max(1, np.searchsorted(ctx, ctx[-1] // 4) + 1))
+
+
+def cpu_baseline(wl, window: int, min_seconds: float = 10.0) -> dict:
+    """The oracle on the host cores (all of them, repeated for about ten seconds)
+    and on one core (a bounded sub-sample, run once)."""
+    threads = oracle_threads()
+    sample = OracleSample(wl, threads, window)
+    gbs, runs, dt = sample.time(min_seconds)
+    one = OracleSample(wl, 1, window, requests=single_thread_requests(wl.cfg))
+    g1, r1, d1 = one.time(0.0)
+    return {"value": gbs / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{sample.description}; {runs} runs in {dt:.1f} s",
+            "seconds": dt,
+            "single_thread": {"value": g1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"{one.description}; {r1} run in {d1:.1f} s",
+                              "seconds": d1}}
 
 
 def run_reference(args):
@@ -285,12 +342,196 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+POOL_MARGIN = 8 << 30  # device bytes kept free beside the pool, cache and step inputs
+
+
+class Setup:
+    """One workload on the GPU: chunk pool, engine (cache, RoPE table, workspace),
+    the context before the step, the step's inputs and its outputs."""
+
+    def __init__(self, cfg, args, dev, rank):
+        import torch
+
+        import workload as W
+        from workload import stage
+        self.cfg = cfg
+        self.wl = wl = W.make_workload(cfg, seed=replica_seed(cfg.seed, rank))
+        torch.cuda.empty_cache()
+        free, _ = torch.cuda.mem_get_info()
+        compact = args.compact_pool or cfg.pool_bytes + wl.cache_bytes + POOL_MARGIN > free
+        remap = None
+        if compact:
+            pool, remap = stage.compact_pool(wl, dev)
+            self.pool_note = ("drawn chunks only" + ("" if args.compact_pool else
+                              f" (the full {cfg.pool_bytes / 1e9:.1f} GB pool does not fit beside "
+                              f"the cache in {free / 1e9:.1f} GB free)"))
+        else:
+            from workload import device as wgen
+            pool = wgen.pool_tensor(wl, dev)
+            self.pool_note = f"full, {cfg.pool_bytes / 1e9:.1f} GB resident"
+        if args.pool_host:
+            # the chunk pool in page-locked host memory: inject reads it over the host link
+            host = torch.empty(pool.shape, dtype=pool.dtype, pin_memory=True)
+            host.copy_(pool)
+            del pool
+            torch.cuda.synchronize()
+            pool = host
+            self.pool_note = "pinned host memory, read in place over the host link; " + self.pool_note
+        self.pool = pool
+        self.eng = eng = stage.make_engine(wl, dev, pool=pool)
+        eng.decode_variant = args.variant
+        eng.overlap_inject = args.overlap_inject
+        eng.window = args.window
+        stage.fill_context(eng, wl, dev)
+        self.inp = stage.step_inputs(wl, dev)
+        if remap is not None:
+            self.inp.chunk_ids.copy_(torch.from_numpy(remap).to(dev))
+        self.out = eng.alloc_outputs(cfg.steps)
+        self.nbytes = stage.algorithmic_bytes(wl, args.window)
+        self.slots = eng.slot_mapping(self.inp.block_tables, self.inp.map_seq, self.inp.map_pos)
+        self.n_inj_tok = self.inp.chunk_ids.numel() * eng.chunk_len
+
+    def inject_only(self):
+        self.eng.inject(self.inp.chunk_ids, self.inp.start_pos, self.slots[:self.n_inj_tok])
+
+    def decode_only(self):
+        """The layer calls as the step makes them (append fused into decode by default;
+        re-appending the same token writes the same bits)."""
+        eng, inp, out, cfg = self.eng, self.inp, self.out, self.cfg
+        for s in range(cfg.steps):
+            for layer in range(cfg.layers):
+                # as in the step: every call after the first follows one on another layer
+                ready = (s > 0 or layer > 0) and cfg.layers > 1
+                if eng.fused_append:
+                    eng.append_decode(layer, inp.q[s, layer], inp.k_new[s, layer],
+                                      inp.v_new[s, layer], inp.q_pos[s], inp.block_tables,
+                                      inp.ctx_lens[s], out[s, layer], kv_ready=ready)
+                else:
+                    eng.decode(layer, inp.q[s, layer], inp.q_pos[s], inp.block_tables,
+                               inp.ctx_lens[s], out[s, layer])
+
+    def release(self):
+        import torch
+        for name in ("eng", "inp", "out", "pool", "slots"):
+            setattr(self, name, None)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
+def graph_ms(fn, reps, use_graph=True):
+    """Average ms of fn (captured in a CUDA graph) over `reps` replays, CUDA events on
+    the launching stream, after two untimed replays."""
+    import torch
+    stream = torch.cuda.current_stream()
+    g = None
+    if use_graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+    run = g.replay if g is not None else fn
+    for _ in range(2):
+        run()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def decode_inject_parts(st: Setup, reps: int, use_graph: bool, peak: float) -> dict:
+    """Per-kernel times of one setup: inject (all layers, one launch) and decode (one
+    call -- split-K pass + combine, with the fused append -- per layer and step)."""
+    cfg, nbytes, eng = st.cfg, st.nbytes, st.eng
+    inj_ms = graph_ms(st.inject_only, reps, use_graph)
+    dec_ms = graph_ms(st.decode_only, reps, use_graph) / (cfg.layers * cfg.steps)
+    dec_bytes = nbytes["decode"] + (nbytes["append"] if eng.fused_append else 0)
+    per_launch = dec_bytes / (cfg.layers * cfg.steps)
+    dec_gbs = per_launch / (dec_ms * 1e-3) / 1e9
+    inj_gbs = nbytes["inject"] / (inj_ms * 1e-3) / 1e9
+    return {
+        "inject": {"tokens_per_s": st.wl.n_inj * cfg.chunk_len / (inj_ms * 1e-3), "gbs": inj_gbs,
+                   "ms": inj_ms, "pct_of_8tbs": 100 * inj_gbs / NOMINAL_HBM_GBS,
+                   "frac_of_measured": inj_gbs / peak, "bytes": nbytes["inject"]},
+        "decode": {"gbs": dec_gbs, "ms_per_layer": dec_ms,
+                   "pct_of_8tbs": 100 * dec_gbs / NOMINAL_HBM_GBS,
+                   "frac_of_measured": dec_gbs / peak, "bytes_per_launch": per_launch},
+    }
+
+
+def time_steps(st: Setup, args, ws, dev, clocks=None):
+    """Time exactly args.steps replays of the captured step (a barrier and a synchronize on
+    both sides); the maximum over ranks. Returns (ms per step, the graph)."""
+    import torch
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    eng, inp, out = st.eng, st.inp, st.out
+    # warm-up (also checks the device status word)
+    for _ in range(args.warmup):
+        eng.step(inp, out)
+    torch.cuda.synchronize()
+    if eng.status.item() != 0:
+        raise RuntimeError(f"device status {eng.status.item():#x} after warm-up")
+    # The timed region replays one CUDA graph of the whole step (the decode loop is
+    # launch-bound from Python otherwise); nothing but the step's own kernels is inside it.
+    g = None if args.no_graph else eng.capture(inp, out)
+    run = g.replay if g is not None else (lambda: eng.step(inp, out))
+    for _ in range(args.warmup):
+        run()
+    barrier()
+    stream = torch.cuda.current_stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if clocks is not None:
+        clocks.__enter__()
+    t0.record(stream)
+    for _ in range(args.steps):
+        run()
+    t1.record(stream)
+    barrier()
+    if clocks is not None:
+        clocks.__exit__(None, None, None)
+    return max_over_ranks(t0.elapsed_time(t1), dev) / args.steps, g
+
+
+def host_link_copy_gbs(st: Setup, max_bytes: int = 2 << 30) -> dict:
+    """Copy rate of the host link for the pool records the inject reads: one copy per
+    drawn chunk record from the page-locked pool into device memory (a ring of device
+    buffers), CUDA events around the copies, at most max_bytes."""
+    import numpy as np
+    import torch
+    pool = st.pool
+    ids = np.unique(st.inp.chunk_ids.cpu().numpy())
+    rec = pool[0].numel() * pool.element_size()
+    n = int(max(1, min(ids.size, max_bytes // rec)))
+    ring = [torch.empty_like(pool[0], device="cuda") for _ in range(min(8, n))]
+    for i in range(min(4, n)):  # warm
+        ring[i % len(ring)].copy_(pool[int(ids[i])], non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(n):
+        ring[i % len(ring)].copy_(pool[int(ids[i])], non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"gbs": n * rec / (ms * 1e-3) / 1e9, "records": n, "record_bytes": rec,
+            "method": "one cudaMemcpyAsync (torch copy_) per drawn chunk record, page-locked "
+                      "host -> device, CUDA events around the copies"}
+
+
 def run_gpu(args):
     import numpy as np
     import torch
 
     import workload as W
-    from workload import stage
 
     ws, rank, local = _dist()
     if ws > 1:
@@ -304,120 +545,19 @@ def run_gpu(args):
     cfg = W.CONFIGS[args.config]
     if args.layers:
         cfg = cfg.scaled(layers=args.layers)  # batch structure does not depend on L
-    wl = W.make_workload(cfg, seed=replica_seed(cfg.seed, rank))  # independent replica per rank
-    remap = None
-    if args.compact_pool:
-        pool, remap = stage.compact_pool(wl, dev)
-    else:
-        from workload import device as wgen
-        pool = wgen.pool_tensor(wl, dev)
-    if args.pool_host:
-        # the chunk pool in page-locked host memory: inject reads it over the host link
-        host = torch.empty(pool.shape, dtype=pool.dtype, pin_memory=True)
-        host.copy_(pool)
-        del pool
-        torch.cuda.synchronize()
-        pool = host
-    eng = stage.make_engine(wl, dev, pool=pool)
-    eng.decode_variant = args.variant
-    eng.overlap_inject = args.overlap_inject
-    eng.window = args.window
-    stage.fill_context(eng, wl, dev)
-    inp = stage.step_inputs(wl, dev)
-    if remap is not None:
-        inp.chunk_ids.copy_(torch.from_numpy(remap).to(dev))
-    out = eng.alloc_outputs(cfg.steps)
-    nbytes = stage.algorithmic_bytes(wl, args.window)
+    peak, peak_kind = _peaks()
+    use_graph = not args.no_graph
+    reps = max(3, args.steps)
+    st = Setup(cfg, args, dev, rank)
+    wl, eng, inp, out, nbytes = st.wl, st.eng, st.inp, st.out, st.nbytes
     stream = torch.cuda.current_stream()
 
-    def barrier():
-        if ws > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-
-    # warm-up (also checks the device status word)
-    for _ in range(args.warmup):
-        eng.step(inp, out)
-    torch.cuda.synchronize()
-    if eng.status.item() != 0:
-        raise RuntimeError(f"device status {eng.status.item():#x} after warm-up")
-
-    # The timed region replays one CUDA graph of the whole step (the decode
-    # loop is launch-bound from Python otherwise); nothing but the step's own
-    # kernels is inside it. Per-kernel times come from separate graphs of the
-    # same launches (inject alone; the L decode launches alone), timed with
-    # events around their replays on the launching stream.
-    use_graph = not args.no_graph
-    g_step = eng.capture(inp, out) if use_graph else None
-
-    def run_step():
-        if g_step is not None:
-            g_step.replay()
-        else:
-            eng.step(inp, out)
-
-    for _ in range(args.warmup):
-        run_step()
-    barrier()
-    with ClockSampler(local) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for k in range(args.steps):
-            run_step()
-        t_end.record(stream)
-        barrier()
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
-    ms_step = elapsed_ms / args.steps
+    clk = ClockSampler(local)
+    ms_step, g_step = time_steps(st, args, ws, dev, clocks=clk)
     value = whole_job_gbs(ws, nbytes["total"], ms_step)
+    parts = decode_inject_parts(st, reps, use_graph, peak)
+    parts["decode"]["tokens_per_s"] = ws * cfg.batch * cfg.steps / (ms_step * 1e-3)
 
-    # per-kernel timing: inject (all layers, one launch) and decode (one
-    # launch pair -- split-K pass + combine -- per layer)
-    slots = eng.slot_mapping(inp.block_tables, inp.map_seq, inp.map_pos)
-    n_inj_tok = inp.chunk_ids.numel() * eng.chunk_len
-
-    def inject_only():
-        eng.inject(inp.chunk_ids, inp.start_pos, slots[:n_inj_tok])
-
-    def decode_only():
-        # the layer calls as the step makes them (append fused into decode by default;
-        # re-appending the same token writes the same bits)
-        for s in range(cfg.steps):
-            for layer in range(cfg.layers):
-                if eng.fused_append:
-                    eng.append_decode(layer, inp.q[s, layer], inp.k_new[s, layer],
-                                      inp.v_new[s, layer], inp.q_pos[s], inp.block_tables,
-                                      inp.ctx_lens[s], out[s, layer])
-                else:
-                    eng.decode(layer, inp.q[s, layer], inp.q_pos[s], inp.block_tables,
-                               inp.ctx_lens[s], out[s, layer])
-
-    def part_ms(fn, reps):
-        g = None
-        if use_graph:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                fn()
-        run = g.replay if g is not None else fn
-        for _ in range(2):
-            run()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
-            run()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / reps
-
-    inj_avg = part_ms(inject_only, max(3, args.steps))
-    dec_avg = part_ms(decode_only, max(3, args.steps)) / (cfg.layers * cfg.steps)
-    dec_bytes = nbytes["decode"] + (nbytes["append"] if eng.fused_append else 0)
-    per_launch_decode = dec_bytes / (cfg.layers * cfg.steps)
-    dec_gbs = per_launch_decode / (dec_avg * 1e-3) / 1e9
-    inj_gbs = nbytes["inject"] / (inj_avg * 1e-3) / 1e9
-    inj_tok_s = wl.n_inj * cfg.chunk_len / (inj_avg * 1e-3)
     # copy-on-write block copies: one call over distinct blocks in use, each copied onto
     # itself (the cache keeps its contents; every record is read and written in full)
     n_copy = min(1024, cfg.batch * max(1, int(wl.context_lens.min()) // cfg.block_size))
@@ -425,11 +565,10 @@ def run_gpu(args):
     n_copy = copy_ids.numel()
     rec_bytes = cfg.kv_heads * cfg.block_size * cfg.head_dim * 2
     copy_bytes = 2 * 2 * n_copy * cfg.layers * rec_bytes  # K and V, read and write
-    copy_avg = part_ms(lambda: eng.copy_blocks(copy_ids, copy_ids), max(3, args.steps))
+    copy_avg = graph_ms(lambda: eng.copy_blocks(copy_ids, copy_ids), reps, use_graph)
     copy_gbs = copy_bytes / (copy_avg * 1e-3) / 1e9
     # paged prefill: the last nq tokens of every context taken as layer 0's query tokens (their
     # K/V are in the cache); each token is a decode row over its own causal context
-    import numpy as np
     ctx_h = wl.context_lens.astype(np.int64) + 1
     nq = int(min(16, ctx_h.min()))
     pos_h = (ctx_h[:, None] - nq + np.arange(nq)[None, :]).reshape(-1)
@@ -438,58 +577,92 @@ def run_gpu(args):
     pf_q = inp.q[0, 0].repeat_interleave(nq, dim=0).contiguous()
     pf_out = torch.empty_like(pf_q)
     eng.prefill(0, pf_q, pf_seq, pf_pos, inp.block_tables, pf_out)  # workspace allocated here
-    pf_avg = part_ms(lambda: eng.prefill(0, pf_q, pf_seq, pf_pos, inp.block_tables, pf_out),
-                     max(3, args.steps))
+    pf_avg = graph_ms(lambda: eng.prefill(0, pf_q, pf_seq, pf_pos, inp.block_tables, pf_out),
+                      reps, use_graph)
     kv_row = cfg.kv_heads * cfg.head_dim * cfg.elem_bytes
     pf_read = int((pos_h + 1).sum()) * 2 * kv_row
     pf_unique = int(ctx_h.sum()) * 2 * kv_row
-    peak, peak_kind = _peaks()
     # slot mapping, inject (one launch, or one per layer when overlapped), then per step and
     # layer the append + decode launches
     inject_launches = cfg.layers if eng.overlap_inject else 1
     launches_per_step = 1 + inject_launches + eng.launches_per_layer() * cfg.layers * cfg.steps
+    link = host_link_copy_gbs(st) if args.pool_host else None
 
     # end to end through host buffers (pinned), same metric
     e2e = None
     if not args.no_e2e:
+        from workload import stage
         host = stage.pinned_copy(inp)
         host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        g0 = g_step
         for _ in range(max(1, args.warmup)):
-            eng.step_from_host(host, inp, out, host_out, g0)
-        barrier()
+            eng.step_from_host(host, inp, out, host_out, g_step)
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.steps):
-            eng.step_from_host(host, inp, out, host_out, g0)
+            eng.step_from_host(host, inp, out, host_out, g_step)
         e1.record(stream)
-        barrier()
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
         e2e = {"value": whole_job_gbs(ws, nbytes["total"], e_ms), "unit": "GB/s",
                "ms_per_step": e_ms, "h2d_bytes_per_step": host.nbytes,
                "d2h_bytes_per_step": host_out.numel() * host_out.element_size()}
+        del host, host_out
     if eng.status.item() != 0:
         raise RuntimeError(f"device status {eng.status.item():#x}")
+    pool_note = st.pool_note
+    # drop every reference to this setup's buffers (the pool alone can be 170+ GB) before
+    # the next workload allocates its own
+    g_step = eng = inp = out = copy_ids = pf_q = pf_out = pf_seq = pf_pos = None
+    st.release()
+
+    # the other workloads the target names, measured in the same run (each step timed the
+    # same way; their per-kernel parts as above)
+    others = {}
+    if not args.no_others and not args.layers:
+        for name in OTHER_WORKLOADS:
+            if name == cfg.name:
+                continue
+            o = Setup(W.CONFIGS[name], args, dev, rank)
+            o_ms, _ = time_steps(o, args, ws, dev)
+            o_val = whole_job_gbs(ws, o.nbytes["total"], o_ms)
+            p = decode_inject_parts(o, reps, use_graph, peak)
+            if o.eng.status.item() != 0:
+                raise RuntimeError(f"{name}: device status {o.eng.status.item():#x}")
+            others[name] = {"value": o_val, "unit": "GB/s", "ms_per_step": o_ms,
+                            "pct_of_8tbs": 100 * o_val / NOMINAL_HBM_GBS,
+                            "frac_of_measured": o_val / peak, "steps": args.steps,
+                            "pool": o.pool_note, "step_bytes": o.nbytes, **p}
+            o.release()
+            del o, p
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        threads = oracle_threads()
-        sample = OracleSample(wl, threads, args.window)
-        # about ten seconds of oracle work: the layer-0 sample, repeated
-        runs, t0 = 0, time.perf_counter()
-        while True:
-            sample.run()
-            runs += 1
-            dt = time.perf_counter() - t0
-            if dt >= 10.0:
-                break
-        cpu = {"value": sample.bytes * runs / dt / 1e9, "unit": "GB/s", "cores": threads,
-               "kind": "oracle", "sample": f"{sample.description}; {runs} runs in {dt:.1f} s",
-               "seconds": dt}
+        cpu = cpu_baseline(wl, args.window)
 
     if rank != 0:
         return
+    parts.update({
+        "prefill": {"query_tokens": int(pos_h.size), "per_request": nq, "layers": 1,
+                    "ms": pf_avg, "tokens_per_s": pos_h.size / (pf_avg * 1e-3),
+                    "kv_bytes_read": pf_read, "gbs": pf_read / (pf_avg * 1e-3) / 1e9,
+                    "unique_kv_bytes": pf_unique,
+                    "note": "each query token a decode row over its causal context; "
+                            "unique bytes are each request's context read once"},
+        "copy_blocks": {"blocks": n_copy, "layers": cfg.layers, "bytes": copy_bytes,
+                        "ms": copy_avg, "gbs": copy_gbs,
+                        "note": "each block copied onto itself: full reads and writes, "
+                                "cache unchanged"},
+        "step_bytes": nbytes,
+        "step_pct_of_8tbs": 100 * value / NOMINAL_HBM_GBS,
+        "other_workloads": others,
+    })
+    inj = parts["inject"]
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -500,42 +673,23 @@ def run_gpu(args):
                           f"step; no flush"),
                    "decode_variant": args.variant,
                    "inject_schedule": ("per layer, low-priority stream beside the decode"
-                                       if eng.overlap_inject else "all layers, then decode"),
+                                       if args.overlap_inject else "all layers, then decode"),
                    "launch": "cuda graph per step" if use_graph else "eager",
-                   "pool": (("pinned host memory, read in place over the host link; "
-                             if args.pool_host else "") +
-                            ("drawn chunks only" if args.compact_pool else
-                             f"full, {cfg.pool_bytes / 1e9:.1f} GB resident"))},
-        "parts": {
-            "inject": {"tokens_per_s": inj_tok_s, "gbs": inj_gbs, "ms": inj_avg,
-                       "pct_of_8tbs": 100 * inj_gbs / NOMINAL_HBM_GBS,
-                       "bytes": nbytes["inject"]},
-            "decode": {"gbs": dec_gbs, "ms_per_layer": dec_avg,
-                       "pct_of_8tbs": 100 * dec_gbs / NOMINAL_HBM_GBS,
-                       "tokens_per_s": ws * cfg.batch * cfg.steps / (ms_step * 1e-3),
-                       "bytes_per_launch": per_launch_decode},
-            "prefill": {"query_tokens": int(pos_h.size), "per_request": nq, "layers": 1,
-                        "ms": pf_avg, "tokens_per_s": pos_h.size / (pf_avg * 1e-3),
-                        "kv_bytes_read": pf_read, "gbs": pf_read / (pf_avg * 1e-3) / 1e9,
-                        "unique_kv_bytes": pf_unique,
-                        "note": "each query token a decode row over its causal context; "
-                                "unique bytes are each request's context read once"},
-            "copy_blocks": {"blocks": n_copy, "layers": cfg.layers, "bytes": copy_bytes,
-                            "ms": copy_avg, "gbs": copy_gbs,
-                            "note": "each block copied onto itself: full reads and writes, "
-                                    "cache unchanged"},
-            "step_bytes": nbytes,
-        },
-        "roofline": {"kernel": "decode", "bound": "hbm", "achieved": dec_gbs, "peak": peak,
-                     "peak_source": peak_kind, "unit": "GB/s", "frac": dec_gbs / peak,
+                   "pool": pool_note},
+        "parts": parts,
+        "roofline": {"kernel": "decode", "bound": "hbm", "achieved": parts["decode"]["gbs"],
+                     "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
+                     "frac": parts["decode"]["gbs"] / peak,
                      "traffic": _traffic_from_profile(f"decode_{cfg.name}")},
         "roofline_inject": ({"kernel": "inject", "bound": "host link (pool reads)",
-                             "achieved": inj_gbs / 2, "peak": None, "unit": "GB/s",
-                             "frac": None, "traffic": None,
+                             "achieved": inj["gbs"] / 2, "peak": link["gbs"],
+                             "peak_source": "measured in this run: " + link["method"],
+                             "unit": "GB/s", "frac": inj["gbs"] / 2 / link["gbs"],
+                             "traffic": None,
                              "note": "achieved = pool bytes read from host memory per second"}
                             if args.pool_host else
-                            {"kernel": "inject", "bound": "hbm", "achieved": inj_gbs,
-                             "peak": peak, "unit": "GB/s", "frac": inj_gbs / peak,
+                            {"kernel": "inject", "bound": "hbm", "achieved": inj["gbs"],
+                             "peak": peak, "unit": "GB/s", "frac": inj["gbs"] / peak,
                              "traffic": _traffic_from_profile(f"inject_{cfg.name}")}),
         "roofline_copy_blocks": {"kernel": "copy_blocks", "bound": "hbm", "achieved": copy_gbs,
                                  "peak": peak, "unit": "GB/s", "frac": copy_gbs / peak,
@@ -571,6 +725,8 @@ def main():
     ap.add_argument("--compact-pool", action="store_true",
                     help="keep only the drawn chunks resident (small profiling cases only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-others", action="store_true",
+                    help="measure the chosen workload only (not the other target workloads)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
