@@ -501,6 +501,39 @@ def time_steps(st: Setup, args, ws, dev, clocks=None):
     return max_over_ranks(t0.elapsed_time(t1), dev) / args.steps, g
 
 
+def measure_int8(st: Setup, args, ws, dev, reps, use_graph, peak, ms16) -> dict:
+    """The same step and per-kernel timings with the KV cache stored as int8 codes and row
+    scales ("Latency Optimization > KV Cache Management", KV cache quantization): an
+    engine with the int8 cache over the same resident pool, the same step inputs; bytes
+    are the int8 cache's (a row: D code bytes + a 4-byte scale)."""
+    import copy
+
+    import torch
+
+    from workload import stage
+    eng = stage.make_engine(st.wl, dev, pool=st.pool, kv="int8")
+    eng.decode_variant = args.variant
+    stage.fill_context(eng, st.wl, dev)
+    s8 = copy.copy(st)
+    s8.eng = eng
+    s8.out = eng.alloc_outputs(st.cfg.steps)
+    s8.nbytes = stage.algorithmic_bytes(st.wl, 0, kv="int8")
+    ms8, g8 = time_steps(s8, args, ws, dev)
+    parts = decode_inject_parts(s8, reps, use_graph, peak)
+    if eng.status.item() != 0:
+        raise RuntimeError(f"int8 cache: device status {eng.status.item():#x}")
+    value = whole_job_gbs(ws, s8.nbytes["total"], ms8)
+    out = {"value": value, "unit": "GB/s", "ms_per_step": ms8,
+           "step_time_vs_16bit": ms8 / ms16, "pct_of_8tbs": 100 * value / NOMINAL_HBM_GBS,
+           "step_bytes": s8.nbytes, **parts,
+           "note": "the step's algorithmic bytes with the cache as int8 codes + one fp32 scale "
+                   "per row; decode turns codes into fp16 tensor-core operands on the chip"}
+    g8 = s8 = eng = None
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def host_link_copy_gbs(st: Setup, max_bytes: int = 2 << 30) -> dict:
     """Copy rate of the host link for the pool records the inject reads: one copy per
     drawn chunk record from the page-locked pool into device memory (a ring of device
@@ -587,6 +620,9 @@ def run_gpu(args):
     inject_launches = cfg.layers if eng.overlap_inject else 1
     launches_per_step = 1 + inject_launches + eng.launches_per_layer() * cfg.layers * cfg.steps
     link = host_link_copy_gbs(st) if args.pool_host else None
+    int8 = None
+    if not args.no_int8 and cfg.head_dim == 128 and cfg.kv_heads % 8 == 0 and not args.window:
+        int8 = measure_int8(st, args, ws, dev, reps, use_graph, peak, ms_step)
 
     # end to end through host buffers (pinned), same metric
     e2e = None
@@ -661,6 +697,7 @@ def run_gpu(args):
         "step_bytes": nbytes,
         "step_pct_of_8tbs": 100 * value / NOMINAL_HBM_GBS,
         "other_workloads": others,
+        "int8_cache": int8,
     })
     inj = parts["inject"]
     line = {
@@ -691,6 +728,11 @@ def run_gpu(args):
                             {"kernel": "inject", "bound": "hbm", "achieved": inj["gbs"],
                              "peak": peak, "unit": "GB/s", "frac": inj["gbs"] / peak,
                              "traffic": _traffic_from_profile(f"inject_{cfg.name}")}),
+        "roofline_decode_int8": ({"kernel": "decode_i8", "bound": "hbm",
+                                  "achieved": int8["decode"]["gbs"], "peak": peak, "unit": "GB/s",
+                                  "frac": int8["decode"]["gbs"] / peak,
+                                  "traffic": _traffic_from_profile(f"decode_i8_{cfg.name}")}
+                                 if int8 else None),
         "roofline_copy_blocks": {"kernel": "copy_blocks", "bound": "hbm", "achieved": copy_gbs,
                                  "peak": peak, "unit": "GB/s", "frac": copy_gbs / peak,
                                  "traffic": _traffic_from_profile(f"copy_blocks_{cfg.name}")},
@@ -725,6 +767,8 @@ def main():
     ap.add_argument("--compact-pool", action="store_true",
                     help="keep only the drawn chunks resident (small profiling cases only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-int8", action="store_true",
+                    help="skip the int8-cache measurement of the chosen workload")
     ap.add_argument("--no-others", action="store_true",
                     help="measure the chosen workload only (not the other target workloads)")
     args = ap.parse_args()

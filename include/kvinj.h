@@ -114,7 +114,31 @@ typedef struct {
   const void *table; /* device float4 [max_pos][head_dim/2] */
   int32_t max_pos;   /* positions 0 .. max_pos-1 are valid */
   int32_t head_dim;
+  const void *table64; /* optional device double2 [max_pos][head_dim/2] {cos, sin} in fp64
+                          (kvinj_rope_table64_host); required by the int8 calls that rotate
+                          keys, ignored by the others (may be NULL there) */
 } kvinj_rope;
+
+/* int8 paged KV cache ("Latency Optimization > KV Cache Management", KV cache
+ * quantization: int8 halves the cache's bytes). Every stored row (one token of
+ * one kv head, D values) is quantized on its own, symmetrically: scale s =
+ * max|x| / 127 as fp32, code = x / s rounded to nearest even and clamped to
+ * [-127, 127] (a row of zeros: s = 0, codes 0); the value read back is code *
+ * s. Keys are rotated first and rounded once to the call's 16-bit type, then
+ * quantized, so a code is the one the fp64 rotation rounded to 16 bits
+ * quantizes to. Same block structure as kvinj_cache; head_dim 128, block_size
+ * 16. */
+typedef struct {
+  int32_t num_layers;   /* L */
+  int32_t num_kv_heads; /* Hkv */
+  int32_t head_dim;     /* D: 128 */
+  int32_t block_size;   /* 16 */
+  int64_t num_blocks;   /* physical blocks per layer */
+  void *k;              /* device int8 codes [L][num_blocks][Hkv][block_size][D], 16-byte aligned */
+  void *v;              /* device int8 codes, same layout */
+  float *k_scale;       /* device fp32 [L][num_blocks][Hkv][block_size], 16-byte aligned */
+  float *v_scale;       /* device fp32, same layout */
+} kvinj_cache_i8;
 
 /* Bytes of the RoPE table for (head_dim, max_pos): max_pos*head_dim/2*16. */
 size_t kvinj_rope_table_bytes(int32_t head_dim, int32_t max_pos);
@@ -126,6 +150,16 @@ size_t kvinj_rope_table_bytes(int32_t head_dim, int32_t max_pos);
  * Returns KVINJ_EINVAL for head_dim odd or <= 0, max_pos <= 0, theta <= 0,
  * out == NULL. */
 int kvinj_rope_table_host(double theta, int32_t head_dim, int32_t max_pos, float *out);
+
+/* Bytes of the fp64 RoPE table for (head_dim, max_pos): max_pos*head_dim/2*16. */
+size_t kvinj_rope_table64_bytes(int32_t head_dim, int32_t max_pos);
+
+/* Fill a HOST buffer of kvinj_rope_table64_bytes() bytes: entry [p][i] holds
+ * {cos, sin} of p * theta^(-2i/head_dim) in fp64 -- the values the float
+ * table's hi/lo pairs are split from. The int8 calls use it where a rotated key
+ * lies so close to a 16-bit rounding boundary that only the fp64 rotation
+ * decides its rounding. Errors as kvinj_rope_table_host. */
+int kvinj_rope_table64_host(double theta, int32_t head_dim, int32_t max_pos, double *out);
 
 /* Slot mapping (InferScale §3.4; "LLM Inference: KV Caching", Paged
  * attention): slot_out[i] = block_tables[seq_ids[i]][positions[i] / B] * B
@@ -348,6 +382,46 @@ int kvinj_paged_decode_static(const kvinj_cache *cache, const kvinj_rope *rope, 
                               const int32_t *block_tables, int32_t max_blocks,
                               const int32_t *context_lens, int32_t batch, float scale, void *out,
                               int32_t *dev_status, kvinj_stream_t stream);
+
+/* Inject into an int8 cache: as kvinj_inject, except that each rotated K row
+ * (rounded once to the pool's 16-bit type, exactly as the fp64 rotation would
+ * be) and each V row is stored as int8 codes with one fp32 scale (see
+ * kvinj_cache_i8). rope->table64 is required (KVINJ_EINVAL without it). The
+ * pool must be device memory; D = 128. */
+int kvinj_inject_i8(const kvinj_pool *pool, const kvinj_cache_i8 *cache, const kvinj_rope *rope,
+                    const int32_t *chunk_ids, const int32_t *start_pos,
+                    const int64_t *slot_mapping, int32_t n_inj, int32_t layer_begin,
+                    int32_t layer_end, int32_t *dev_status, kvinj_stream_t stream);
+
+/* Append into an int8 cache: as kvinj_append (k_new, v_new: device [n][Hkv][D]
+ * of 16-bit type `dtype`), the rows quantized as kvinj_inject_i8 stores them.
+ * With rope, rope->table64 is required; rope == NULL stores K as given. */
+int kvinj_append_i8(const kvinj_cache_i8 *cache, const kvinj_rope *rope, int32_t dtype,
+                    int32_t layer, const void *k_new, const void *v_new,
+                    const int32_t *positions, const int64_t *slot_mapping, int64_t n,
+                    int32_t *dev_status, kvinj_stream_t stream);
+
+/* Paged decode over an int8 cache ("Latency Optimization > KV Cache
+ * Management", KV cache quantization; attention as kvinj_paged_decode), with
+ * the new token's append fused when k_new and v_new are both given (as
+ * kvinj_append_paged_decode: the token at q_pos[r] is quantized and written at
+ * the slot its block table gives, then attended to). Each key and value is
+ * read back as code * scale of its row: scores are (q' . codes) * k_scale,
+ * and each probability is multiplied by its row's v_scale before the sum over
+ * values, in fp32. q, out, k_new, v_new are of 16-bit type `dtype`
+ * ([batch][Hq][D], [batch][Hkv][D]). Workspace as kvinj_paged_decode
+ * (kvinj_decode_workspace_size). Requires D = 128, block_size 16, Hkv a
+ * multiple of 8 and G = Hq/Hkv in {1, 2, 4, 8} (KVINJ_EUNSUPPORTED
+ * otherwise); `ctas` as in kvinj_paged_decode_ex; with a fused append and a
+ * rope, rope->table64 is required. Two kernels on `stream`: the split-K pass
+ * (which turns each unit's codes into tensor-core operands on the chip) and
+ * the combine pass. */
+int kvinj_paged_decode_i8(const kvinj_cache_i8 *cache, const kvinj_rope *rope, int32_t dtype,
+                          int32_t layer, int32_t num_q_heads, const void *q, const void *k_new,
+                          const void *v_new, const int32_t *q_pos, const int32_t *block_tables,
+                          int32_t max_blocks, const int32_t *context_lens, int32_t batch,
+                          float scale, void *out, void *workspace, size_t ws_bytes,
+                          int32_t *dev_status, kvinj_stream_t stream, int32_t ctas);
 
 /* KV bytes of `tokens` tokens: 2 * layers * heads * head_dim * tokens *
  * bytes_per_elem ("LLM Inference: KV Caching", What the cache costs). */

@@ -120,6 +120,42 @@ int make_cache_map(CUtensorMap *m, void *base, const kvinj_cache *c, int HG) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? KVINJ_OK : KVINJ_ECUDA; }
 
+int check_cache_i8(const kvinj_cache_i8 *c) {
+  if (!c || !c->k || !c->v || !c->k_scale || !c->v_scale) return KVINJ_EINVAL;
+  if (!aligned16(c->k) || !aligned16(c->v) || !aligned16(c->k_scale) || !aligned16(c->v_scale))
+    return KVINJ_EINVAL;
+  if (c->num_layers <= 0 || c->num_kv_heads <= 0 || c->num_blocks <= 0) return KVINJ_EINVAL;
+  if (c->head_dim != 128 || c->block_size != 16) return KVINJ_EUNSUPPORTED;
+  if ((int64_t)c->num_layers * c->num_blocks * c->num_kv_heads * 16 >= (int64_t)1 << 31)
+    return KVINJ_EUNSUPPORTED;
+  return KVINJ_OK;
+}
+
+// int8 codes as a 2-D tensor: rows of 128 bytes, box 128 bytes x `rows` rows, 128-byte
+// swizzle (the converters read each row's 16-byte chunks at chunk ^ (row % 8))
+int make_code_map(CUtensorMap *m, void *base, const kvinj_cache_i8 *c, int rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return KVINJ_ECUDA;
+  const uint64_t n = (uint64_t)c->num_layers * (uint64_t)c->num_blocks *
+                     (uint64_t)c->num_kv_heads * (uint64_t)c->block_size;
+  cuuint64_t dims[2] = {(cuuint64_t)c->head_dim, (cuuint64_t)n};
+  cuuint64_t strides[1] = {(cuuint64_t)c->head_dim};
+  cuuint32_t box[2] = {128, (cuuint32_t)rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KVINJ_OK : KVINJ_ECUDA;
+}
+
+// a rope for the int8 calls that rotate keys: both tables
+int check_rope64(const kvinj_rope *r, int D) {
+  int rc = check_rope(r, D);
+  if (rc) return rc;
+  if (!r->table64 || !aligned16(r->table64)) return KVINJ_EINVAL;
+  return KVINJ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -144,6 +180,27 @@ int kvinj_rope_table_host(double theta, int32_t head_dim, int32_t max_pos, float
       e[1] = sh;
       e[2] = (float)(c - (double)ch);
       e[3] = (float)(s - (double)sh);
+    }
+  }
+  return KVINJ_OK;
+}
+
+size_t kvinj_rope_table64_bytes(int32_t head_dim, int32_t max_pos) {
+  if (head_dim <= 0 || max_pos <= 0) return 0;
+  return (size_t)max_pos * (size_t)(head_dim / 2) * 2 * sizeof(double);
+}
+
+int kvinj_rope_table64_host(double theta, int32_t head_dim, int32_t max_pos, double *out) {
+  if (!out || head_dim <= 0 || (head_dim & 1) || max_pos <= 0 || !(theta > 0.0))
+    return KVINJ_EINVAL;
+  const int half = head_dim / 2;
+  for (int i = 0; i < half; ++i) {
+    const double inv_freq = pow(theta, -(double)(2 * i) / (double)head_dim);
+    for (int64_t p = 0; p < max_pos; ++p) {
+      const double ang = (double)p * inv_freq;
+      double *e = out + ((size_t)p * half + i) * 2;
+      e[0] = cos(ang);
+      e[1] = sin(ang);
     }
   }
   return KVINJ_OK;
@@ -498,6 +555,148 @@ int kvinj_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t
   return kvinj_paged_decode_ex(cache, rope, layer, num_q_heads, q, q_pos, block_tables,
                                max_blocks, context_lens, batch, scale, out, workspace, ws_bytes,
                                dev_status, stream, 0, 0, 0);
+}
+
+int kvinj_inject_i8(const kvinj_pool *pool, const kvinj_cache_i8 *cache, const kvinj_rope *rope,
+                    const int32_t *chunk_ids, const int32_t *start_pos,
+                    const int64_t *slot_mapping, int32_t n_inj, int32_t layer_begin,
+                    int32_t layer_end, int32_t *dev_status, kvinj_stream_t stream) {
+  int rc = check_cache_i8(cache);
+  if (rc) return rc;
+  if (!pool || !pool->data || !aligned16(pool->data) || !dtype_ok(pool->dtype)) return KVINJ_EINVAL;
+  if (pool->num_layers != cache->num_layers || pool->num_kv_heads != cache->num_kv_heads ||
+      pool->head_dim != cache->head_dim || pool->chunk_len <= 0 || pool->num_chunks <= 0)
+    return KVINJ_EINVAL;
+  if ((rc = check_rope64(rope, cache->head_dim))) return rc;
+  if (n_inj < 0 || layer_begin < 0 || layer_end > cache->num_layers || layer_begin > layer_end)
+    return KVINJ_EINVAL;
+  if (n_inj == 0 || layer_begin == layer_end) return KVINJ_OK;
+  if (!chunk_ids || !start_pos || !slot_mapping) return KVINJ_EINVAL;
+  const void *pool_dev = device_view(pool->data);
+  if (pool_dev != pool->data) return KVINJ_EINVAL;  // device memory only
+  I8Args a = {};
+  a.src_k = static_cast<const uint16_t *>(pool->data);
+  a.L = cache->num_layers;
+  a.Hkv = cache->num_kv_heads;
+  a.chunk_len = pool->chunk_len;
+  a.num_chunks = pool->num_chunks;
+  a.k = static_cast<int8_t *>(cache->k);
+  a.v = static_cast<int8_t *>(cache->v);
+  a.ks = cache->k_scale;
+  a.vs = cache->v_scale;
+  a.num_blocks = cache->num_blocks;
+  a.B = cache->block_size;
+  a.rope = static_cast<const float4 *>(rope->table);
+  a.rope64 = static_cast<const double2 *>(rope->table64);
+  a.max_pos = rope->max_pos;
+  a.chunk_ids = chunk_ids;
+  a.start_pos = start_pos;
+  a.slot_mapping = slot_mapping;
+  a.n = n_inj;
+  a.layer_begin = layer_begin;
+  a.n_layers = layer_end - layer_begin;
+  a.status = dev_status;
+  return cuda_rc(launch_inject_i8(a, pool->dtype, (cudaStream_t)stream));
+}
+
+int kvinj_append_i8(const kvinj_cache_i8 *cache, const kvinj_rope *rope, int32_t dtype,
+                    int32_t layer, const void *k_new, const void *v_new,
+                    const int32_t *positions, const int64_t *slot_mapping, int64_t n,
+                    int32_t *dev_status, kvinj_stream_t stream) {
+  int rc = check_cache_i8(cache);
+  if (rc) return rc;
+  if (!dtype_ok(dtype)) return KVINJ_EINVAL;
+  if (rope && (rc = check_rope64(rope, cache->head_dim))) return rc;
+  if (n < 0 || layer < 0 || layer >= cache->num_layers) return KVINJ_EINVAL;
+  if (n == 0) return KVINJ_OK;
+  if (!k_new || !v_new || !positions || !slot_mapping) return KVINJ_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new)) return KVINJ_EINVAL;
+  I8Args a = {};
+  a.src_k = static_cast<const uint16_t *>(k_new);
+  a.src_v = static_cast<const uint16_t *>(v_new);
+  a.Hkv = cache->num_kv_heads;
+  a.k = static_cast<int8_t *>(cache->k);
+  a.v = static_cast<int8_t *>(cache->v);
+  a.ks = cache->k_scale;
+  a.vs = cache->v_scale;
+  a.num_blocks = cache->num_blocks;
+  a.B = cache->block_size;
+  a.rope = rope ? static_cast<const float4 *>(rope->table) : nullptr;
+  a.rope64 = rope ? static_cast<const double2 *>(rope->table64) : nullptr;
+  a.max_pos = rope ? rope->max_pos : 0;
+  a.positions = positions;
+  a.slot_mapping = slot_mapping;
+  a.n = n;
+  a.layer = layer;
+  a.status = dev_status;
+  return cuda_rc(launch_append_i8(a, dtype, (cudaStream_t)stream));
+}
+
+int kvinj_paged_decode_i8(const kvinj_cache_i8 *cache, const kvinj_rope *rope, int32_t dtype,
+                          int32_t layer, int32_t num_q_heads, const void *q, const void *k_new,
+                          const void *v_new, const int32_t *q_pos, const int32_t *block_tables,
+                          int32_t max_blocks, const int32_t *context_lens, int32_t batch,
+                          float scale, void *out, void *workspace, size_t ws_bytes,
+                          int32_t *dev_status, kvinj_stream_t stream, int32_t ctas) {
+  int rc = check_cache_i8(cache);
+  if (rc) return rc;
+  if (!dtype_ok(dtype)) return KVINJ_EINVAL;
+  const int D = cache->head_dim, Hkv = cache->num_kv_heads;
+  const bool append = k_new != nullptr || v_new != nullptr;
+  if (append && (!k_new || !v_new || !q_pos || !aligned16(k_new) || !aligned16(v_new)))
+    return KVINJ_EINVAL;
+  if (rope) {
+    if ((rc = append ? check_rope64(rope, D) : check_rope(rope, D))) return rc;
+  }
+  if (layer < 0 || layer >= cache->num_layers || batch < 0 || max_blocks <= 0) return KVINJ_EINVAL;
+  if (num_q_heads <= 0 || num_q_heads % Hkv) return KVINJ_EINVAL;
+  const int G = num_q_heads / Hkv;
+  if (batch == 0) return KVINJ_OK;
+  if (!q || !block_tables || !context_lens || !out || !workspace) return KVINJ_EINVAL;
+  if (rope && !q_pos) return KVINJ_EINVAL;
+  if (!aligned16(q) || !aligned16(out)) return KVINJ_EINVAL;
+  if (decode_head_group(Hkv) != 8 || !(G == 1 || G == 2 || G == 4 || G == 8))
+    return KVINJ_EUNSUPPORTED;
+  if ((int64_t)batch * Hkv * max_blocks >= (int64_t)1 << 31) return KVINJ_EUNSUPPORTED;
+  if (batch > 4096) return KVINJ_EUNSUPPORTED;
+  if (ws_bytes < kvinj_decode_workspace_size(batch, num_q_heads, Hkv, D)) return KVINJ_EWORKSPACE;
+  const int max_ctas = decode_max_ctas();
+  if (ctas < 0 || ctas > max_ctas) return KVINJ_EINVAL;
+  if (ctas == 0) ctas = num_sms();
+  CUtensorMap tmK, tmV;
+  const int box_rows = G == 8 ? 16 : 128;  // one head of one block, or a block of 8 heads
+  if ((rc = make_code_map(&tmK, cache->k, cache, box_rows))) return rc;
+  if ((rc = make_code_map(&tmV, cache->v, cache, box_rows))) return rc;
+  DecodeArgs a = {};
+  a.q = static_cast<const uint16_t *>(q);
+  a.q_pos = q_pos;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.rope = rope ? static_cast<const float4 *>(rope->table) : nullptr;
+  a.rope64 = rope ? static_cast<const double2 *>(rope->table64) : nullptr;
+  a.max_pos = rope ? rope->max_pos : 0;
+  a.out = static_cast<uint16_t *>(out);
+  a.desc = static_cast<int *>(workspace);
+  a.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + decode_desc_bytes());
+  a.k_new = static_cast<const uint16_t *>(k_new);
+  a.v_new = static_cast<const uint16_t *>(v_new);
+  a.k_cache = static_cast<uint16_t *>(cache->k);
+  a.v_cache = static_cast<uint16_t *>(cache->v);
+  a.k_scale = cache->k_scale;
+  a.v_scale = cache->v_scale;
+  a.status = dev_status;
+  a.batch = batch;
+  a.Hq = num_q_heads;
+  a.Hkv = Hkv;
+  a.max_blocks = max_blocks;
+  a.layer = layer;
+  a.num_blocks = cache->num_blocks;
+  a.ctas = ctas;
+  a.window = 0;
+  a.early = 0;
+  const double sc = scale > 0.f ? (double)scale : 1.0 / sqrt((double)D);
+  a.scale_log2 = (float)(sc * 1.4426950408889634);
+  return cuda_rc(launch_decode_i8(a, tmK, tmV, G, dtype, ctas, (cudaStream_t)stream));
 }
 
 int64_t kvinj_kv_bytes(int32_t layers, int32_t heads, int32_t head_dim, int64_t tokens,

@@ -43,6 +43,8 @@ struct DecodeLayout {
   static constexpr int BPU = 1;               // 16-token blocks per unit
   static constexpr bool SPLIT_KV = false;     // K and V of a stage share one barrier pair
   static constexpr int VR = S;                // valid bits: one entry per stage
+  static constexpr bool I8 = false;           // 16-bit cache
+  static constexpr int CODE_BYTES = 0, SC_BYTES = 0, STAGE_TX = 0;
   static constexpr int off_qfull = 0, QBUF = 1;
   static constexpr int NBOX = D / 64;                   // 64-element (128-byte) column boxes
   static constexpr int BOXB = HG * BLK * 128;           // bytes of one box: HG*16 rows
@@ -451,7 +453,38 @@ __device__ void decode_producer(const DecodeArgs &a, const CUtensorMap &tmK,
                                 (j ? r1 : r0) + h * BLK, bar);
             }
           };
-          if constexpr (Lay::SPLIT_KV) {
+          if constexpr (Lay::I8) {
+            // int8 cache: the K and V code tiles (the 128-byte swizzle, like the 16-bit
+            // tiles' column blocks) and the rows' K and V scales, all on one barrier
+            uint8_t *sc = kd + 2 * Lay::CODE_BYTES;
+            mbar_arrive_expect_tx(full + st, Lay::STAGE_TX);
+            if constexpr (Lay::BPU == 1) {
+              tma_load_2d(kd, &tmK, 0, r0, full + st);
+              tma_load_2d(kd + Lay::CODE_BYTES, &tmV, 0, r0, full + st);
+              bulk_load(sc, a.k_scale + r0, Lay::SC_BYTES, full + st);
+              bulk_load(sc + Lay::SC_BYTES, a.v_scale + r0, Lay::SC_BYTES, full + st);
+            } else {
+              // rows in (head, block, token) order, one 16-row box per (head, block); the
+              // scales of block j are copied as [j][head][token]
+#pragma unroll
+              for (int h = 0; h < HG; ++h)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                  tma_load_2d(kd + (h * 2 + j) * BLK * 128, &tmK, 0, (j ? r1 : r0) + h * BLK,
+                              full + st);
+                  tma_load_2d(kd + Lay::CODE_BYTES + (h * 2 + j) * BLK * 128, &tmV, 0,
+                              (j ? r1 : r0) + h * BLK, full + st);
+                }
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                bulk_load(sc + j * (Lay::SC_BYTES / 2), a.k_scale + (j ? r1 : r0),
+                          Lay::SC_BYTES / 2, full + st);
+                bulk_load(sc + Lay::SC_BYTES + j * (Lay::SC_BYTES / 2), a.v_scale + (j ? r1 : r0),
+                          Lay::SC_BYTES / 2, full + st);
+              }
+            }
+            kiss = viss = gi + 1;
+          } else if constexpr (Lay::SPLIT_KV) {
             // K is released once its QK is done, V once its PV is: K runs ahead of V
             mbar_arrive_expect_tx(full + st, Lay::UNIT_BYTES);
             load_half(kd, &tmK, full + st);

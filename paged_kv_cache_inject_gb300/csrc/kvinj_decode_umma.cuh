@@ -100,6 +100,8 @@ struct UmmaLayout {
   // ring, as unit gi's entry is written when its K is issued (after QK(gi - S)), when the
   // softmax has read the entries of units up to gi - S - 2
   static constexpr int VR = SPLIT_KV ? 8 : S;
+  static constexpr bool I8 = false;          // 16-bit cache
+  static constexpr int CODE_BYTES = 0, SC_BYTES = 0, STAGE_TX = 0;
   static constexpr bool QPOS_SM = true;      // the query warps read q positions there
   static constexpr bool APPEND_WAIT = true;  // the producer waits for a fused append
   static constexpr int N = HG * 2 * G;       // MMA N

@@ -72,6 +72,106 @@ __device__ __forceinline__ float2 rope_pair(float a, float b, float4 t) {
 }
 
 // ---------------------------------------------------------------------------
+// Exactly rounded rotation (the int8 paths). The stored 16-bit key must be the
+// rounding of the fp64 rotation a*c - b*s, b*c + a*s (products and sum each
+// rounded in fp64) with c, s the fp64 table values: the int8 code of a row
+// depends on every bit of it. rope_pair's fp32 result y differs from the exact
+// a*C - b*S (C, S = the hi + lo table values) by less than 2^-23|y| +
+// 2^-44(|a| + |b|), and C, S differ from the fp64 values by less than 2^-48,
+// so with E = 2^-22|y| + 2^-43(|a| + |b|) the fp64 result lies in
+// [y - E, y + E]. When both ends of that interval round to the same 16-bit
+// value, so does the fp64 result; otherwise (a rounding boundary inside the
+// interval, about 2^-14 of the elements for bf16) the rotation is recomputed
+// in fp64 from the fp64 table, with the fp64 operations in the same order.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __forceinline__ uint16_t f32_to16(float x) {
+  if constexpr (DT == 0) return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  else return __half_as_ushort(__float2half_rn(x));
+}
+
+// round-to-nearest-even of an fp64 value to the 16-bit type: round to odd into
+// fp32 (truncate; set the last bit when inexact), then to nearest even -- the
+// same result as a single rounding, fp32 carrying more than two extra bits
+// (Boldo and Melquiond, "Emulation of FMA and correctly rounded sums: proved
+// algorithms using rounding to odd", IEEE Trans. Computers 57(4), 2008)
+template <int DT>
+__device__ __forceinline__ uint16_t f64_to16(double x) {
+  float f = __double2float_rz(x);
+  if ((double)f != x) f = __uint_as_float(__float_as_uint(f) | 1u);
+  return f32_to16<DT>(f);
+}
+
+template <int DT>
+__device__ __forceinline__ bool rounds_alike(float y, float e) {
+  return f32_to16<DT>(__fsub_rd(y, e)) == f32_to16<DT>(__fadd_ru(y, e));
+}
+
+// bf16: whether every value within 2^-22|y| + 2^-43(|a| + |b|) of y rounds as y does, from
+// y's bits alone in the common case: a bf16 rounding boundary is an fp32 whose low 16 bits
+// are 0x8000, so |low16 - 0x8000| is y's distance to the nearest one in fp32 ulps of y;
+// 2^-22|y| is under 4 of those ulps, and 2^-43(|a| + |b|) under one while |y| >= 2^-18
+// (|a| + |b|). Anything else (near a boundary, heavy cancellation, zero) reports false and
+// takes the exact path.
+__device__ __forceinline__ bool bf16_rounding_safe(float y, float ab) {
+  const uint32_t t = __float_as_uint(y);
+  const int d = abs((int)(t & 0xFFFFu) - 0x8000);
+  return d > 6 && fabsf(y) > 0x1p-18f * ab;
+}
+
+// rotated pair (a, b) at the position whose table entries are t (float hi/lo)
+// and *t64 (fp64 {cos, sin}), each output rounded once to the 16-bit type
+template <int DT>
+__device__ __forceinline__ ushort2 rope_pair_exact(float a, float b, float4 t,
+                                                   const double2 *t64) {
+  const float2 y = rope_pair(a, b, t);
+  const float ab = fabsf(a) + fabsf(b);
+  bool safe;
+  if constexpr (DT == 0) {
+    safe = bf16_rounding_safe(y.x, ab) && bf16_rounding_safe(y.y, ab);
+  } else {
+    const float base = 0x1p-43f * ab;
+    safe = rounds_alike<DT>(y.x, __fmaf_ru(0x1p-22f, fabsf(y.x), base)) &&
+           rounds_alike<DT>(y.y, __fmaf_ru(0x1p-22f, fabsf(y.y), base));
+  }
+  if (safe) return make_ushort2(f32_to16<DT>(y.x), f32_to16<DT>(y.y));
+  const double2 cs = *t64;
+  const double da = a, db = b;
+  const double r0 = __dsub_rn(__dmul_rn(da, cs.x), __dmul_rn(db, cs.y));
+  const double r1 = __dadd_rn(__dmul_rn(db, cs.x), __dmul_rn(da, cs.y));
+  return make_ushort2(f64_to16<DT>(r0), f64_to16<DT>(r1));
+}
+
+// ---------------------------------------------------------------------------
+// int8 row quantization ("Latency Optimization > KV Cache Management", KV cache
+// quantization): s = max|x| / 127 rounded to fp32 (one correctly rounded fp32
+// division gives the fp64 quotient's fp32 rounding here: the quotient of a
+// 16-bit value by 127 never lies within the fp64 rounding error of an fp32
+// rounding boundary), code = x / s rounded to nearest even, clamped to
+// [-127, 127]. The code is decided exactly: c0 = rint(x * (1/s)) is within one
+// of it (the product is within 2^-16 of the quotient, which is below 128), and
+// the signs of x - (c0 +- 1/2) s, each computed with one fma (rounding keeps the
+// sign and keeps zero as zero), say whether the exact quotient lies past a
+// half-way point or on it. inv = the row's 1/s (any nearby value will do).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float quant_scale(float amax) { return __fdiv_rn(amax, 127.f); }
+__device__ __forceinline__ float quant_inv(float s) { return s > 0.f ? __frcp_rn(s) : 0.f; }
+
+__device__ __forceinline__ int quant_code(float x, float s, float inv) {
+  if (!(s > 0.f)) return 0;
+  const float q = x * inv, c0 = rintf(q);
+  // the product is within 2^-16 of the quotient: away from a half-way point c0 is the code
+  if (fabsf(q - c0) < 0.4995f) return min(max((int)c0, -127), 127);
+  const float hi = __fmaf_rn(-(c0 + 0.5f), s, x);  // x - (c0 + 1/2) s
+  const float lo = __fmaf_rn(-(c0 - 0.5f), s, x);  // x - (c0 - 1/2) s
+  const int ci = (int)c0, odd = ci & 1;
+  int c = ci;
+  if (hi > 0.f || (hi == 0.f && odd)) c = ci + 1;        // past c0 + 1/2, or a tie: the even one
+  else if (lo < 0.f || (lo == 0.f && odd)) c = ci - 1;
+  return min(max(c, -127), 127);
+}
+
+// ---------------------------------------------------------------------------
 // cache-hinted global memory access
 // ---------------------------------------------------------------------------
 template <int BYTES>

@@ -62,12 +62,35 @@ struct DecodeArgs {
                                // may be read before the dependency wait (KVINJ_DECODE_KV_READY)
   int64_t num_blocks;
   float scale_log2;            // softmax scale times log2(e)
+  // int8 cache (kvinj_paged_decode_i8): k_cache/v_cache hold int8 codes, these the scales
+  float *k_scale, *v_scale;    // [L][num_blocks][Hkv][16]
+  const double2 *rope64;       // fp64 table: exact rounding of the appended key
 };
 
 // decode workspace: descriptors first, then the partial slots
 size_t decode_partial_floats(int G, int D);  // floats per head of a slot
 int decode_max_ctas();                        // slots/2 the workspace is sized for
 size_t decode_desc_bytes();
+
+// int8 cache (inject / append): codes [L][NB][Hkv][B][D], scales [L][NB][Hkv][B]
+struct I8Args {
+  const uint16_t *src_k, *src_v;  // inject: the pool; append: k_new, v_new [n][Hkv][D]
+  int L, Hkv, chunk_len;          // inject: pool geometry
+  int64_t num_chunks;
+  int8_t *k, *v;
+  float *ks, *vs;
+  int64_t num_blocks;
+  int B;
+  const float4 *rope;             // nullptr (append only): keys stored as given
+  const double2 *rope64;          // fp64 {cos, sin} of the same positions
+  int max_pos;
+  const int32_t *chunk_ids, *start_pos;  // inject
+  const int32_t *positions;              // append
+  const int64_t *slot_mapping;
+  int64_t n;                      // inject: injected chunks; append: tokens
+  int layer, layer_begin, n_layers;
+  int32_t *status;
+};
 
 cudaError_t launch_slot_mapping(const int32_t *bt, int max_blocks, int batch, int64_t num_blocks,
                                 int B, const int32_t *seq, const int32_t *pos, int64_t n,
@@ -104,6 +127,11 @@ cudaError_t launch_decode_mma(const DecodeArgs &a, const CUtensorMap &tmK, const
 cudaError_t launch_decode_umma(const DecodeArgs &a, const CUtensorMap &tmK,
                                const CUtensorMap &tmV, int D, int G, int HG, int dtype, int ctas,
                                cudaStream_t s);
+// int8 cache: inject / append (D = 128), decode (tcgen05; D = 128, HG = 8, G in {1,2,4,8})
+cudaError_t launch_inject_i8(const I8Args &a, int dtype, cudaStream_t s);
+cudaError_t launch_append_i8(const I8Args &a, int dtype, cudaStream_t s);
+cudaError_t launch_decode_i8(const DecodeArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                             int G, int dtype, int ctas, cudaStream_t s);
 // variant: 1 = CUDA-core FMA kernel, 2 = mma.sync kernel, 3 = tcgen05 kernel
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmV,
                           int D, int G, int HG, int dtype, int variant, int ctas, cudaStream_t s);

@@ -47,15 +47,28 @@ class StepInputs:
 
 
 class Engine:
+    """kv: "16" keeps the cache in the pool's 16-bit type; "int8" keeps it as int8 codes with
+    one fp32 scale per row ("Latency Optimization > KV Cache Management", KV cache
+    quantization), written by kvinj_inject_i8 / kvinj_append_i8 and read by
+    kvinj_paged_decode_i8 (D = 128; block copies, prefill and the sliding window are
+    16-bit calls)."""
+
     def __init__(self, *, layers: int, q_heads: int, kv_heads: int, head_dim: int,
                  block_size: int, dtype: torch.dtype, num_blocks: int, max_pos: int,
-                 theta: float, batch: int, pool: torch.Tensor, device="cuda"):
+                 theta: float, batch: int, pool: torch.Tensor, device="cuda", kv: str = "16"):
         self.L, self.Hq, self.Hkv, self.D, self.B = layers, q_heads, kv_heads, head_dim, block_size
         self.dtype, self.batch, self.device = dtype, batch, device
+        assert kv in ("16", "int8")
+        self.kv = kv
         shape = (layers, num_blocks, kv_heads, block_size, head_dim)
-        self.k_cache = torch.empty(shape, dtype=dtype, device=device)
-        self.v_cache = torch.empty(shape, dtype=dtype, device=device)
-        self.cache = K.Cache(self.k_cache, self.v_cache)
+        if kv == "int8":
+            self.k_cache = self.v_cache = None
+            self.cache = K.CacheI8.empty(layers, num_blocks, kv_heads, head_dim, block_size,
+                                         device)
+        else:
+            self.k_cache = torch.empty(shape, dtype=dtype, device=device)
+            self.v_cache = torch.empty(shape, dtype=dtype, device=device)
+            self.cache = K.Cache(self.k_cache, self.v_cache)
         self.pool = K.Pool(pool)
         self.chunk_len = pool.shape[3]
         self.rope = K.make_rope(theta, head_dim, max_pos, device)
@@ -82,10 +95,18 @@ class Engine:
                                     self.status)
 
     def inject(self, chunk_ids, start_pos, slots, layer_begin=0, layer_end=None):
+        if self.kv == "int8":
+            K.kvinj_inject_i8(self.pool, self.cache, self.rope, chunk_ids, start_pos, slots,
+                              layer_begin, layer_end, self.status)
+            return
         K.kvinj_inject(self.pool, self.cache, self.rope, chunk_ids, start_pos, slots,
                        layer_begin, layer_end, self.status)
 
     def append(self, layer, k_new, v_new, positions, slots, rotate=True):
+        if self.kv == "int8":
+            K.kvinj_append_i8(self.cache, self.rope if rotate else None, layer, k_new, v_new,
+                              positions, slots, self.status)
+            return
         K.kvinj_append(self.cache, self.rope if rotate else None, layer, k_new, v_new,
                        positions, slots, self.status)
 
@@ -94,6 +115,11 @@ class Engine:
         before the previous decode call on the stream, which was on another layer
         (KVINJ_DECODE_KV_READY: the call may stream pages before the kernel ahead ends)."""
         flags = K.KVINJ_DECODE_KV_READY if kv_ready and self.early_kv else 0
+        if self.kv == "int8":
+            K.kvinj_paged_decode_i8(self.cache, self.rope if rotate else None, layer, q, q_pos,
+                                    block_tables, ctx_lens, out, self.workspace,
+                                    status=self.status, ctas=self.decode_ctas)
+            return
         if self.window:
             K.kvinj_paged_decode_window(self.cache, self.rope if rotate else None, layer, q, q_pos,
                                         block_tables, ctx_lens, self.window, out, self.workspace,
@@ -107,6 +133,11 @@ class Engine:
                       rotate=True, kv_ready=False):
         """Append + decode in one call; kv_ready as in decode()."""
         flags = K.KVINJ_DECODE_KV_READY if kv_ready and self.early_kv else 0
+        if self.kv == "int8":
+            K.kvinj_paged_decode_i8(self.cache, self.rope if rotate else None, layer, q, q_pos,
+                                    block_tables, ctx_lens, out, self.workspace, k_new=k_new,
+                                    v_new=v_new, status=self.status, ctas=self.decode_ctas)
+            return
         if self.window:
             K.kvinj_paged_decode_window(self.cache, self.rope if rotate else None, layer, q, q_pos,
                                         block_tables, ctx_lens, self.window, out, self.workspace,
@@ -133,7 +164,9 @@ class Engine:
         K.kvinj_copy_blocks(self.cache, src, dst, layer_begin, layer_end, self.status)
 
     def uses_tcgen05(self) -> bool:
-        """Whether decode runs the tcgen05 kernel (one launch per layer)."""
+        """Whether decode runs a tcgen05 kernel (one launch per layer)."""
+        if self.kv == "int8":
+            return True
         G = self.Hq // self.Hkv
         ok = self.D == 128 and self.Hkv % 8 == 0 and G in (1, 2, 4, 8)  # the automatic choice
         return self.decode_variant == 3 or (self.decode_variant == 0 and ok)

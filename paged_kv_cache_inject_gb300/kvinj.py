@@ -32,7 +32,8 @@ EXPORTS = [
     "kvinj_paged_decode", "kvinj_paged_decode_ex", "kvinj_append_paged_decode",
     "kvinj_append_paged_decode_ex", "kvinj_paged_decode_static", "kvinj_kv_bytes",
     "kvinj_strerror", "kvinj_copy_blocks", "kvinj_paged_decode_window",
-    "kvinj_prefill_workspace_size", "kvinj_paged_prefill",
+    "kvinj_prefill_workspace_size", "kvinj_paged_prefill", "kvinj_rope_table64_bytes",
+    "kvinj_rope_table64_host", "kvinj_inject_i8", "kvinj_append_i8", "kvinj_paged_decode_i8",
 ]
 
 
@@ -58,7 +59,14 @@ class _Pool(ctypes.Structure):
 
 class _Rope(ctypes.Structure):
     _fields_ = [("table", ctypes.c_void_p), ("max_pos", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32)]
+                ("head_dim", ctypes.c_int32), ("table64", ctypes.c_void_p)]
+
+
+class _CacheI8(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int64), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 _lib = None
@@ -104,6 +112,12 @@ def load(path: str = LIB_PATH):
             "kvinj_paged_decode_static": (ctypes.c_int, [P, P, i32, i32, P, P, P, i32, P, i32,
                                                          ctypes.c_float, P, P, P]),
             "kvinj_kv_bytes": (i64, [i32, i32, i32, i64, i32]),
+            "kvinj_rope_table64_bytes": (sz, [i32, i32]),
+            "kvinj_rope_table64_host": (ctypes.c_int, [ctypes.c_double, i32, i32, P]),
+            "kvinj_inject_i8": (ctypes.c_int, [P, P, P, P, P, P, i32, i32, i32, P, P]),
+            "kvinj_append_i8": (ctypes.c_int, [P, P, i32, i32, P, P, P, P, i64, P, P]),
+            "kvinj_paged_decode_i8": (ctypes.c_int, [P, P, i32, i32, i32, P, P, P, P, P, i32, P,
+                                                     i32, ctypes.c_float, P, P, sz, P, P, i32]),
             "kvinj_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
@@ -142,6 +156,37 @@ class Cache:
         return ctypes.byref(self._s)
 
 
+class CacheI8:
+    """int8 paged cache: codes k, v int8 [L][num_blocks][Hkv][16][D], scales k_scale,
+    v_scale float32 [L][num_blocks][Hkv][16], on the GPU."""
+
+    def __init__(self, k: torch.Tensor, v: torch.Tensor, k_scale: torch.Tensor,
+                 v_scale: torch.Tensor):
+        assert k.shape == v.shape and k.dim() == 5 and k.dtype == v.dtype == torch.int8
+        assert k_scale.shape == v_scale.shape == k.shape[:4]
+        assert k_scale.dtype == v_scale.dtype == torch.float32
+        for t in (k, v, k_scale, v_scale):
+            assert t.is_cuda and t.is_contiguous()
+        self.k, self.v, self.k_scale, self.v_scale = k, v, k_scale, v_scale
+        L, NB, Hkv, B, D = k.shape
+        self.num_layers, self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim = \
+            L, NB, Hkv, B, D
+        self._s = _CacheI8(L, Hkv, D, B, NB, k.data_ptr(), v.data_ptr(), k_scale.data_ptr(),
+                           v_scale.data_ptr())
+
+    @classmethod
+    def empty(cls, layers, num_blocks, kv_heads, head_dim, block_size=16, device="cuda"):
+        shape = (layers, num_blocks, kv_heads, block_size, head_dim)
+        return cls(torch.empty(shape, dtype=torch.int8, device=device),
+                   torch.empty(shape, dtype=torch.int8, device=device),
+                   torch.empty(shape[:4], dtype=torch.float32, device=device),
+                   torch.empty(shape[:4], dtype=torch.float32, device=device))
+
+    @property
+    def ref(self):
+        return ctypes.byref(self._s)
+
+
 class Pool:
     """Pre-RoPE chunk pool: data [num_chunks][L][2][chunk_len][Hkv][D] on the GPU, or in
     page-locked host memory (a pinned CPU tensor), which inject reads in place."""
@@ -159,14 +204,20 @@ class Pool:
 
 
 class Rope:
-    """RoPE table (float4 [max_pos][D/2]) on the GPU."""
+    """RoPE table (float4 [max_pos][D/2]) on the GPU, with the fp64 table (double2
+    [max_pos][D/2] {cos, sin}) the int8 calls that rotate keys also need."""
 
-    def __init__(self, table: torch.Tensor, head_dim: int):
+    def __init__(self, table: torch.Tensor, head_dim: int, table64: torch.Tensor | None = None):
         assert table.is_cuda and table.dtype == torch.float32 and table.is_contiguous()
         self.table = table
+        self.table64 = table64
         self.max_pos = table.shape[0]
         self.head_dim = head_dim
-        self._s = _Rope(table.data_ptr(), self.max_pos, head_dim)
+        if table64 is not None:
+            assert table64.is_cuda and table64.dtype == torch.float64 and table64.is_contiguous()
+            assert table64.shape[0] == self.max_pos
+        self._s = _Rope(table.data_ptr(), self.max_pos, head_dim,
+                        table64.data_ptr() if table64 is not None else None)
 
     @property
     def ref(self):
@@ -212,10 +263,22 @@ def kvinj_rope_table_host(theta: float, head_dim: int, max_pos: int) -> np.ndarr
     return out
 
 
+def kvinj_rope_table64_host(theta: float, head_dim: int, max_pos: int) -> np.ndarray:
+    """Host table float64 [max_pos][head_dim/2][2] = {cos, sin}."""
+    out = np.empty((max_pos, head_dim // 2, 2), np.float64)
+    _check("kvinj_rope_table64_host",
+           load().kvinj_rope_table64_host(float(theta), head_dim, max_pos,
+                                          out.ctypes.data_as(ctypes.c_void_p)))
+    return out
+
+
 def make_rope(theta: float, head_dim: int, max_pos: int, device="cuda") -> Rope:
-    """Build the table on the host (fp64) and copy it to the device."""
+    """Build the tables on the host (fp64) and copy them to the device: the float hi/lo
+    table every rotation uses and the fp64 one the int8 calls also need."""
     host = kvinj_rope_table_host(theta, head_dim, max_pos)
-    return Rope(torch.from_numpy(host).to(device).contiguous(), head_dim)
+    host64 = kvinj_rope_table64_host(theta, head_dim, max_pos)
+    return Rope(torch.from_numpy(host).to(device).contiguous(), head_dim,
+                torch.from_numpy(host64).to(device).contiguous())
 
 
 def kvinj_slot_mapping(block_tables, seq_ids, positions, num_blocks: int, block_size: int,
@@ -378,4 +441,44 @@ def kvinj_append_paged_decode(cache: Cache, rope: Rope | None, layer: int, q, k_
                _ptr(context_lens), batch, float(scale), _ptr(out), _ptr(workspace),
                workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream),
                variant, ctas, int(flags)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# int8 cache
+# ---------------------------------------------------------------------------
+def kvinj_inject_i8(pool: Pool, cache: CacheI8, rope: Rope, chunk_ids, start_pos, slot_mapping,
+                    layer_begin: int = 0, layer_end: int | None = None, status=None,
+                    stream=None):
+    """Inject into an int8 cache: each rotated K row and each V row quantized."""
+    le = cache.num_layers if layer_end is None else layer_end
+    _check("kvinj_inject_i8",
+           load().kvinj_inject_i8(pool.ref, cache.ref, rope.ref, _ptr(chunk_ids),
+                                  _ptr(start_pos), _ptr(slot_mapping), chunk_ids.numel(),
+                                  layer_begin, le, _ptr(status), _stream(stream)))
+
+
+def kvinj_append_i8(cache: CacheI8, rope: Rope | None, layer: int, k_new, v_new, positions,
+                    slot_mapping, status=None, stream=None):
+    """Append k_new, v_new [n][Hkv][D] (16-bit) at their slots, quantized."""
+    _check("kvinj_append_i8",
+           load().kvinj_append_i8(cache.ref, rope.ref if rope is not None else None,
+                                  _dtype_code(k_new.dtype), layer, _ptr(k_new), _ptr(v_new),
+                                  _ptr(positions), _ptr(slot_mapping), positions.numel(),
+                                  _ptr(status), _stream(stream)))
+
+
+def kvinj_paged_decode_i8(cache: CacheI8, rope: Rope | None, layer: int, q, q_pos,
+                          block_tables, context_lens, out, workspace, k_new=None, v_new=None,
+                          scale: float = 0.0, status=None, stream=None, ctas: int = 0):
+    """Paged decode over an int8 cache (q, out [batch][Hq][D] 16-bit), with the new token's
+    append fused when k_new and v_new are given."""
+    batch, Hq, _ = q.shape
+    _check("kvinj_paged_decode_i8",
+           load().kvinj_paged_decode_i8(
+               cache.ref, rope.ref if rope is not None else None, _dtype_code(q.dtype), layer,
+               Hq, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(q_pos), _ptr(block_tables),
+               block_tables.shape[1], _ptr(context_lens), batch, float(scale), _ptr(out),
+               _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+               _stream(stream), ctas))
     return out

@@ -85,3 +85,37 @@ def expected_decode(wl: W.Workload, step: int, layer: int, r: int, qh: int):
     K, V = expected_cache_rows(wl, layer, r, np.arange(n), h)
     q = wl.q_rows(step, layer)[r, qh]
     return oracle.attention_bits(q, n - 1, cfg.theta, K, V, cfg.dtype)
+
+
+def expected_request_rows(wl: W.Workload, layer: int, r: int, n: int):
+    """(K bits, V bits) [Hkv][n][D] the cache must hold for request r's first n positions."""
+    ks, vs = [], []
+    for h in range(wl.cfg.kv_heads):
+        k, v = expected_cache_rows(wl, layer, r, np.arange(n), h)
+        ks.append(k)
+        vs.append(v)
+    return np.stack(ks), np.stack(vs)
+
+
+def request_cache(k_rows: np.ndarray, v_rows: np.ndarray):
+    """A one-request paged cache [1][NB][Hkv][16][D] (and its table) holding rows
+    [Hkv][n][D] contiguously, for the oracle's paged decode."""
+    Hkv, n, D = k_rows.shape
+    NB = -(-n // 16)
+    kc = np.zeros((1, NB * 16, Hkv, D), k_rows.dtype)
+    vc = np.zeros_like(kc)
+    kc[0, :n] = k_rows.transpose(1, 0, 2)
+    vc[0, :n] = v_rows.transpose(1, 0, 2)
+    kc = kc.reshape(1, NB, 16, Hkv, D).transpose(0, 1, 3, 2, 4).copy()
+    vc = vc.reshape(1, NB, 16, Hkv, D).transpose(0, 1, 3, 2, 4).copy()
+    return kc, vc, np.arange(NB, dtype=np.int32)[None]
+
+
+def gpu_request_rows(cache_k: np.ndarray, cache_v: np.ndarray, layer: int, bt_row: np.ndarray,
+                     n: int):
+    """Rows [Hkv][n][...] of a request's first n positions gathered from host copies of the
+    GPU cache ([L][NB][Hkv][16][...]) through its block table (values: plain indexing)."""
+    p = np.arange(n)
+    blk = bt_row[p // 16]
+    return cache_k[layer, blk, :, p % 16].transpose(1, 0, 2), \
+        cache_v[layer, blk, :, p % 16].transpose(1, 0, 2)

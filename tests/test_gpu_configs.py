@@ -1,24 +1,34 @@
 """The five workloads at full size, in the launch configuration the benchmark
-times, checked against the oracle on sampled outputs.
+times, checked against the oracle.
 
 For each workload: the chunk pool and the preceding context are put on the
 GPU, one full step runs (slot mapping, inject over all layers, then per
 decode step and layer: append + paged decode), and then
   - every slot the step mapped is compared bit for bit with the oracle's,
-  - sampled cache rows (injected, appended and step tokens) match the
-    oracle's rotated keys within one ulp and its values bit for bit,
-  - sampled decode outputs match the oracle within atol 2e-3 + rtol 1e-2.
-Also: the device generator reproduces the host generator's bits."""
+  - every cache row of the last layer (injected, appended and step tokens)
+    matches the oracle's rotated keys within one ulp and its values bit for
+    bit,
+  - every output of the first and the last layer at the first and the last
+    decode step (every request, every query head) matches the oracle within
+    atol 2e-3 + rtol 1e-2.
+The int8 cache runs the same step on two workloads and is checked the same
+way against the oracle's quantization and int8 decode. Also: the device
+generator reproduces the host generator's bits."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import workload as W
-from tests.gpu_helpers import (assert_decode_close, bits, expected_cache_rows, expected_decode,
-                               ulp_distance)
+from tests.gpu_helpers import (assert_decode_close, bits, expected_request_rows, gpu_request_rows,
+                               request_cache, ulp_distance)
 
 pytestmark = pytest.mark.gpu
+
+
+def oracle_threads():
+    import os
+    return (os.cpu_count() or 1) if oracle.has_openmp() else 1
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -87,34 +97,36 @@ def test_config_full_size(name):
     assert st == 0
     assert np.array_equal(slots.cpu().numpy(), want)
 
-    # sampled cache rows: injected, appended and step tokens of every kind
-    B, D = cfg.block_size, cfg.head_dim
-    n_rows = 256 if cfg.layers > 1 else 64
+    # every cache row of the last layer (K within one ulp of the oracle's rotation, V bit
+    # for bit), and every output of the first and last layer at the first and last decode
+    # step, each against the oracle's attention over the request's rows
+    L = cfg.layers
+    layers = sorted({0, L - 1})
+    steps = sorted({0, cfg.steps - 1})
+    gk = bits(eng.k_cache[L - 1]).reshape((1,) + tuple(eng.k_cache.shape[1:]))
+    gv = bits(eng.v_cache[L - 1]).reshape((1,) + tuple(eng.v_cache.shape[1:]))
+    got_all = {(s, l): out[s, l].float().cpu().numpy().astype(np.float64)
+               for s in steps for l in layers}
     worst = 0
-    for _ in range(n_rows):
-        r = int(rng.integers(cfg.batch))
-        n = int(wl.context_lens[r]) + cfg.steps
-        p = int(rng.integers(n))
-        layer, h = int(rng.integers(cfg.layers)), int(rng.integers(cfg.kv_heads))
-        k_want, v_want = expected_cache_rows(wl, layer, r, [p], h)
-        blk = int(wl.block_tables[r, p // B])
-        k_got = bits(eng.k_cache[layer, blk, h, p % B])
-        v_got = bits(eng.v_cache[layer, blk, h, p % B])
-        assert np.array_equal(v_got, v_want[0]), (r, p, layer, h)
-        d = ulp_distance(k_got, k_want[0])
-        worst = max(worst, int(d.max()))
+    for layer in layers:
+        for r in range(cfg.batch):
+            n_max = int(wl.context_lens[r]) + cfg.steps
+            k_want, v_want = expected_request_rows(wl, layer, r, n_max)
+            if layer == L - 1:
+                k_got, v_got = gpu_request_rows(gk, gv, 0, wl.block_tables[r], n_max)
+                assert np.array_equal(v_got, v_want), (name, r)
+                worst = max(worst, int(ulp_distance(k_got, k_want).max()))
+            for s in steps:
+                n = int(wl.context_lens[r]) + s + 1
+                kc, vc, bt1 = request_cache(k_want[:, :n], v_want[:, :n])
+                q = wl.q_rows(s, layer)[r:r + 1]
+                want, st = oracle.paged_decode(kc, vc, 0, q, np.array([n - 1], np.int32), bt1,
+                                               np.array([n], np.int32), cfg.theta, cfg.dtype,
+                                               n_threads=oracle_threads())
+                assert st == 0
+                assert_decode_close(got_all[(s, layer)][r], want[0],
+                                    f"{name} step {s} layer {layer} req {r}")
     assert worst <= 1
-
-    # sampled decode outputs: the longest request, the shortest, and random ones
-    order = np.argsort(wl.context_lens)
-    reqs = [int(order[-1]), int(order[0])] + [int(x) for x in rng.integers(cfg.batch, size=6)]
-    for i, r in enumerate(reqs):
-        s = cfg.steps - 1 if i % 2 == 0 else int(rng.integers(cfg.steps))
-        layer = int(rng.integers(cfg.layers))
-        qh = int(rng.integers(cfg.q_heads))
-        want = expected_decode(wl, s, layer, r, qh)
-        got = out[s, layer, r, qh].float().cpu().numpy().astype(np.float64)
-        assert_decode_close(got, want, f"{name} step {s} layer {layer} req {r} head {qh}")
     del eng, pool, inp, out
     torch.cuda.empty_cache()
 
@@ -177,3 +189,52 @@ def test_early_page_reads_match_waiting_calls_bitwise(name, ctas, window):
         del eng, g
     for a, b in zip(*results):
         assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("name,layers,steps", [("llama3_8b_b32", 4, 1), ("llama3_70b_b8_8k", 2, 3)])
+def test_int8_cache_step_matches_oracle(name, layers, steps):
+    # the whole step with the int8 cache (inject, then per step and layer the fused append +
+    # decode), graph-captured as timed: every cache row of the last layer holds the oracle's
+    # codes and scales, and every output of the first and last layer at the first and last
+    # step matches the oracle's int8 decode over those codes
+    from workload import stage
+    cfg = W.CONFIGS[name].scaled(layers=layers, steps=steps)
+    wl = W.make_workload(cfg)
+    pool, remap = stage.compact_pool(wl)
+    eng = stage.make_engine(wl, pool=pool, kv="int8")
+    stage.fill_context(eng, wl)
+    inp = stage.step_inputs(wl)
+    inp.chunk_ids.copy_(torch.from_numpy(remap).cuda())
+    out = eng.alloc_outputs(cfg.steps)
+    g = eng.capture(inp, out)
+    g.replay()
+    torch.cuda.synchronize()
+    assert eng.status.item() == 0
+    L = cfg.layers
+    c = eng.cache
+    gkq = c.k[L - 1:].cpu().numpy()
+    gvq = c.v[L - 1:].cpu().numpy()
+    gks = c.k_scale[L - 1:].cpu().numpy()[..., None]
+    gvs = c.v_scale[L - 1:].cpu().numpy()[..., None]
+    for layer in sorted({0, L - 1}):
+        for r in range(cfg.batch):
+            n_max = int(wl.context_lens[r]) + cfg.steps
+            k16, v16 = expected_request_rows(wl, layer, r, n_max)
+            kq, ks = oracle.quantize_rows_i8(k16, cfg.dtype)
+            vq, vs = oracle.quantize_rows_i8(v16, cfg.dtype)
+            if layer == L - 1:
+                a, b = gpu_request_rows(gkq, gvq, 0, wl.block_tables[r], n_max)
+                assert np.array_equal(a, kq) and np.array_equal(b, vq), (name, r)
+                a, b = gpu_request_rows(gks, gvs, 0, wl.block_tables[r], n_max)
+                assert np.array_equal(a[..., 0], ks) and np.array_equal(b[..., 0], vs), (name, r)
+            for s in sorted({0, cfg.steps - 1}):
+                n = int(wl.context_lens[r]) + s + 1
+                kc, vc, bt1 = request_cache(kq[:, :n], vq[:, :n])
+                ksc, vsc, _ = request_cache(ks[:, :n, None], vs[:, :n, None])
+                want, st = oracle.paged_decode_i8(kc, ksc[..., 0], vc, vsc[..., 0], 0,
+                                                  wl.q_rows(s, layer)[r:r + 1],
+                                                  np.array([n - 1], np.int32), bt1,
+                                                  np.array([n], np.int32), cfg.theta, cfg.dtype)
+                assert st == 0
+                got = out[s, layer, r].float().cpu().numpy().astype(np.float64)
+                assert_decode_close(got, want[0], f"int8 {name} step {s} layer {layer} req {r}")

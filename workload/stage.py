@@ -16,14 +16,16 @@ from . import Workload
 from . import device as gen
 
 
-def make_engine(wl: Workload, device="cuda", pool: torch.Tensor | None = None) -> Engine:
+def make_engine(wl: Workload, device="cuda", pool: torch.Tensor | None = None,
+                kv: str = "16") -> Engine:
     cfg = wl.cfg
     if pool is None:
         pool = gen.pool_tensor(wl, device)
     return Engine(layers=cfg.layers, q_heads=cfg.q_heads, kv_heads=cfg.kv_heads,
                   head_dim=cfg.head_dim, block_size=cfg.block_size,
                   dtype=gen.torch_dtype(cfg.dtype), num_blocks=wl.num_blocks,
-                  max_pos=wl.max_pos, theta=cfg.theta, batch=cfg.batch, pool=pool, device=device)
+                  max_pos=wl.max_pos, theta=cfg.theta, batch=cfg.batch, pool=pool, device=device,
+                  kv=kv)
 
 
 def compact_pool(wl: Workload, device="cuda"):
@@ -96,7 +98,7 @@ def pinned_copy(inp: StepInputs) -> StepInputs:
     return StepInputs(*[t.cpu().pin_memory() for t in inp.tensors()])
 
 
-def algorithmic_bytes(wl: Workload, window: int = 0) -> dict:
+def algorithmic_bytes(wl: Workload, window: int = 0, kv: str = "16") -> dict:
     """Bytes one step must move at minimum, per part (the roofline numerator).
 
     inject: read the injected chunks' K/V rows and write them to the cache,
@@ -104,13 +106,16 @@ def algorithmic_bytes(wl: Workload, window: int = 0) -> dict:
     append: the same per new token and layer, read + write;
     decode: read every context token's K and V once per layer and step (under a sliding
             window of `window` tokens only the last `window`), plus q, out and the
-            block-table entries of the pages read."""
+            block-table entries of the pages read.
+    With the int8 cache (kv = "int8") a cached row is D code bytes and a 4-byte scale
+    instead of D 16-bit values: reads of the 16-bit pool and new tokens stay 16-bit."""
     cfg = wl.cfg
     b = cfg.elem_bytes
-    row = cfg.kv_heads * cfg.head_dim * b
+    row16 = cfg.kv_heads * cfg.head_dim * b
+    row = cfg.kv_heads * (cfg.head_dim + 4) if kv == "int8" else row16
     n_inj_tok = wl.n_inj * cfg.chunk_len
-    inject = 2 * 2 * cfg.layers * row * n_inj_tok
-    append = 2 * 2 * row * cfg.batch * cfg.layers * cfg.steps
+    inject = 2 * cfg.layers * (row16 + row) * n_inj_tok
+    append = 2 * (row16 + row) * cfg.batch * cfg.layers * cfg.steps
     decode = 0
     for s in range(cfg.steps):
         ctx = wl.context_lens.astype(np.int64) + s + 1
