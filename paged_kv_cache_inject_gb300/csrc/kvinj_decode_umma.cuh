@@ -86,6 +86,10 @@ constexpr float UMMA_TAU = 8.f;  // lazy-maximum threshold, log2 units
 template <bool EARLY, int BPU>
 constexpr bool UMMA_COMBINE_RELEASE_EARLY = EARLY;
 
+// softmax warp sets of the kernel at a given G (two halve each softmax thread's query heads)
+template <int G>
+constexpr int UMMA_SOFTMAX_SETS = G >= 2 ? 2 : 1;
+
 template <int G_, int S_, int QBUF_, int HG_ = 8, int BPU_ = 1>
 struct UmmaLayout {
   static constexpr int D = 128, G = G_, HG = HG_, S = S_;
@@ -123,9 +127,9 @@ struct UmmaLayout {
   static constexpr int off_qfull = off_xbar + 6 * 8;  // qfull[QBUF] (see below)
   static constexpr int off_valid = off_xbar + NXBAR * 8;  // [VR] valid bits
   static constexpr int off_qinfo = off_valid + VR * 4;  // unused (no bytes)
-  static constexpr int off_flags = off_qinfo;          // [0] abort [1] unused [8..16) scan
-  static constexpr int off_alpha = off_flags + 64;     // [2][N] factors, [2][4] flags
-  static constexpr int off_ml = off_alpha + 2 * N * 4 + 32;
+  static constexpr int off_flags = off_qinfo;          // [0] abort [1] unused [8..20) scan
+  static constexpr int off_alpha = off_flags + 96;     // [2][N] factors, [2][8] flags
+  static constexpr int off_ml = off_alpha + 2 * N * 4 + 64;
   static constexpr int off_tmem = off_ml + 2 * HG * G * 4;
   static constexpr int off_pre = off_tmem + 16;        // pre[batch + 1], then qpos[batch]
   // S[2] at columns 0 and N, O at 2N
@@ -156,15 +160,22 @@ __device__ __forceinline__ void sts128_zero(uint32_t addr) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
 }
 
-// warps: 0 producer, 1 MMA issuer and TMEM owner, 2-3 queries, 4-7 softmax
-constexpr int UMMA_THREADS = 256;
+// warps: 0 producer, 1 MMA issuer and TMEM owner, 2-3 queries, then SW sets of four softmax
+// warps (set k: warps 4 + 4k .. 7 + 4k, query heads g in [k G/SW, (k + 1) G/SW) of each kv
+// head, the same TMEM lanes as the other sets)
+template <int SW>
+constexpr int umma_threads() { return 128 + 128 * SW; }
 
-template <int G, int S, int QBUF, int DT, int HG = 8, int BPU = 1, bool EARLY = false>
-__global__ void __launch_bounds__(UMMA_THREADS, 1)
+template <int G, int S, int QBUF, int DT, int HG = 8, int BPU = 1, bool EARLY = false,
+          int SW = 1>
+__global__ void __launch_bounds__(umma_threads<SW>(), 1)
     decode_umma_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, DecodeArgs a) {
   using Lay = UmmaLayout<G, S, QBUF, HG, BPU>;
   constexpr int D = 128, N = Lay::N, PF = partial_floats(G, D), SLOT = HG * PF;
+  constexpr int NT = umma_threads<SW>();
+  constexpr int GS = G / SW;       // query heads per kv head of one softmax set
+  static_assert(SW == 1 || (SW == 2 && G >= 2 && HG % 2 == 0), "softmax sets");
   constexpr int TPH = BLK * BPU;   // tokens of a head in a unit (its rows are consecutive)
   constexpr int HPW = 32 / TPH;    // heads per softmax warp
   static_assert(G == 1 || G == 2 || G == 4 || G == 8, "tcgen05 decode: G");
@@ -189,15 +200,15 @@ __global__ void __launch_bounds__(UMMA_THREADS, 1)
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(sfull + b, 1);
-      mbar_init(sfree + b, 4);
+      mbar_init(sfree + b, 4 * SW);
     }
-    mbar_init(pfull, 4);
+    mbar_init(pfull, 4 * SW);
     mbar_init(pvdone, 1);
     for (int b = 0; b < QBUF; ++b) {
       mbar_init(qfull + b, 2);
       mbar_init(qempty + b, 1);
     }
-    mbar_init(ofree, 4);
+    mbar_init(ofree, 4 * SW);
     mbar_init(done, 1);
     fence_mbar_init();
   }
@@ -206,15 +217,14 @@ __global__ void __launch_bounds__(UMMA_THREADS, 1)
     tmem_relinquish();
   }
   CtaRange rg;
-  const bool has_units = decode_prologue<Lay, UMMA_THREADS, EARLY>(a, sm, rg);
+  const bool has_units = decode_prologue<Lay, NT, EARLY>(a, sm, rg);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (!has_units) {
     if constexpr (EARLY) {
       decode_dependency_wait();
-      zero_invalid_outputs<128>(a, reinterpret_cast<const int *>(sm + Lay::off_pre), tid,
-                                UMMA_THREADS);
+      zero_invalid_outputs<128>(a, reinterpret_cast<const int *>(sm + Lay::off_pre), tid, NT);
     }
     if (warp == 1) tmem_dealloc(*tslot, Lay::TMEM_COLS);
     return;
@@ -228,7 +238,7 @@ __global__ void __launch_bounds__(UMMA_THREADS, 1)
       decode_dependency_wait();
       if (warp >= 4)
         zero_invalid_outputs<128>(a, reinterpret_cast<const int *>(sm + Lay::off_pre), tid - 128,
-                                  128);
+                                  NT - 128);
     }
   }
   const uint32_t tbase = *tslot;
@@ -422,9 +432,12 @@ __global__ void __launch_bounds__(UMMA_THREADS, 1)
       P = pc.end;
       ++piece;
     }
-  } else {
+  } else if (warp < 4 + 4 * SW) {
     // -------------------------------- softmax --------------------------------
     const int qd = warp & 3;            // TMEM lane quadrant
+    const int set = SW == 1 ? 0 : (warp - 4) >> 2;  // softmax set: heads g0 .. g0 + GS - 1
+    const int g0 = set * GS;
+    const int hh0 = set * (HG / SW);    // kv heads whose O columns this set rescales and reads
     const int row = 32 * qd + lane;     // unit row = head * 16 + token; O row = dimension
     // unit row = (head, token of the unit): head h owns rows TPH*h .. TPH*h + TPH-1
     const int hs = lane / TPH, h = HPW * qd + hs, t = lane % TPH;
@@ -433,16 +446,16 @@ __global__ void __launch_bounds__(UMMA_THREADS, 1)
     float *m_sm = reinterpret_cast<float *>(sm + Lay::off_ml), *l_sm = m_sm + HG * G;
     const int *valid = reinterpret_cast<const int *>(sm + Lay::off_valid);
     // the P tile's off-diagonal blocks stay zero
-    for (int i = tid - 128; i < Lay::TILE_BYTES / 16; i += 128) sts128_zero(p0 + 16 * i);
+    for (int i = tid - 128; i < Lay::TILE_BYTES / 16; i += 128 * SW) sts128_zero(p0 + 16 * i);
     fence_async_smem();
 
     int P = rg.b0, gi0 = 0;
     while (P < rg.b1) {
       const Piece pc = find_piece<BPU>(a, pre, ngrp, P, rg.b1);
       const int np = pc.end - P;
-      float m_run[G], l_part[G];
+      float m_run[GS], l_part[GS];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
+      for (int g = 0; g < GS; ++g) {
         m_run[g] = -INFINITY;
         l_part[g] = 0.f;
       }
@@ -458,29 +471,33 @@ __global__ void __launch_bounds__(UMMA_THREADS, 1)
         const int tok = (pc.pg0 + j) * TPH + t;
         const bool live = ok && ((valid[Lay::SPLIT_KV ? gi % Lay::VR : st] >> (t / BLK)) & 1) &&
                           tok < pc.ctx && tok >= pc.lo;
-        float s[G];
+        float s[GS];
         if (ok) {
           tc_fence_after();
           uint32_t r[HPW * 2 * G];
           tmem_ld<HPW * 2 * G>(tmem_addr(tbase + par * N, 32 * qd, HPW * 2 * G * qd), r);
-#pragma unroll
-          for (int g = 0; g < G; ++g)
-            s[g] = (HPW == 2 && hs) ? __uint_as_float(r[(2 * G + g) % (HPW * 2 * G)]) +
+          // (register indices stay compile-time: a set picks its half by a select)
+          auto score = [&](int g) {
+            return (HPW == 2 && hs) ? __uint_as_float(r[(2 * G + g) % (HPW * 2 * G)]) +
                                           __uint_as_float(r[(3 * G + g) % (HPW * 2 * G)])
                                     : __uint_as_float(r[g]) + __uint_as_float(r[G + g]);
+          };
+#pragma unroll
+          for (int gl = 0; gl < GS; ++gl)
+            s[gl] = (SW == 2 && set) ? score(GS + gl) : score(gl);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(sfree + par);
         if (!live) {
 #pragma unroll
-          for (int g = 0; g < G; ++g) s[g] = -INFINITY;
+          for (int g = 0; g < GS; ++g) s[g] = -INFINITY;
         }
         // unit maximum per query head; move m only past the threshold
-        float alpha[G], p[G];
+        float alpha[GS], p[GS];
         bool resc = false;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int g = 0; g < GS; ++g) {
           float mu = s[g];
 #pragma unroll
           for (int o = 1; o < TPH; o <<= 1) mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, o));
@@ -495,16 +512,18 @@ __global__ void __launch_bounds__(UMMA_THREADS, 1)
         }
         if (t == 0) {
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            alpha_sm[par * N + h * 2 * G + g] = alpha[g];
-            alpha_sm[par * N + h * 2 * G + G + g] = alpha[g];
+          for (int g = 0; g < GS; ++g) {
+            alpha_sm[par * N + h * 2 * G + g0 + g] = alpha[g];
+            alpha_sm[par * N + h * 2 * G + G + g0 + g] = alpha[g];
           }
         }
         const int any = __any_sync(0xffffffffu, resc);
-        if (lane == 0) rflag[par * 4 + qd] = any;
-        named_bar_sync(1, 128);
-        const bool need =
-            j > 0 && (rflag[par * 4] | rflag[par * 4 + 1] | rflag[par * 4 + 2] | rflag[par * 4 + 3]);
+        if (lane == 0) rflag[par * 8 + set * 4 + qd] = any;
+        named_bar_sync(1, 128 * SW);
+        int anyr = 0;
+#pragma unroll
+        for (int f = 0; f < 4 * SW; ++f) anyr |= rflag[par * 8 + f];
+        const bool need = j > 0 && anyr;
         // PV of the previous unit done: the P tile is free and O is current
         bool okpv = true;
         if (j > 0) {
@@ -512,9 +531,10 @@ __global__ void __launch_bounds__(UMMA_THREADS, 1)
           if (okpv) tc_fence_after();
         }
         if (need && okpv) {
-          // O row `row` (dimension), every column times its factor
+          // O row `row` (dimension), every column of this set's kv heads times its factor
 #pragma unroll
-          for (int hh = 0; hh < HG; ++hh) {
+          for (int k = 0; k < HG / SW; ++k) {
+            const int hh = hh0 + k;
             uint32_t o[2 * G];
             const uint32_t ta = tmem_addr(tbase + 2 * N, 32 * qd, hh * 2 * G);
             tmem_ld<2 * G>(ta, o);
@@ -526,22 +546,25 @@ __global__ void __launch_bounds__(UMMA_THREADS, 1)
         }
         // P^T: column k = row of this thread, rows n = (h, g, hi | lo)
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const uint16_t hi = to16<DT>(p[g]);
+        for (int gl = 0; gl < GS; ++gl) {
+          const int g = g0 + gl;
+          const uint16_t hi = to16<DT>(p[gl]);
           const float hf = DT == 0 ? __bfloat162float(__ushort_as_bfloat16(hi))
                                    : __half2float(__ushort_as_half(hi));
-          const uint16_t lo = to16<DT>(p[g] - hf);
+          const uint16_t lo = to16<DT>(p[gl] - hf);
           sts16(p0 + tile_off<N>(h * 2 * G + g, row), hi);
           sts16(p0 + tile_off<N>(h * 2 * G + G + g, row), lo);
         }
         // V rows past the context may hold anything (even NaN bit patterns):
-        // zero them so that 0 * V stays 0
+        // zero them so that 0 * V stays 0 (each set its column boxes)
         if (!live) {
           const uint32_t vr = stage0 + st * Lay::STAGE_BYTES + Lay::UNIT_BYTES + row * 128;
 #pragma unroll
           for (int b = 0; b < Lay::NBOX; ++b)
+            if (b % SW == set) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) sts128_zero(vr + b * Lay::BOXB + 16 * c);
+              for (int c = 0; c < 8; ++c) sts128_zero(vr + b * Lay::BOXB + 16 * c);
+            }
         }
         fence_async_smem();
         tc_fence_before();
@@ -550,9 +573,9 @@ __global__ void __launch_bounds__(UMMA_THREADS, 1)
       }
 
       // ---- end of piece: outputs or the partial state ----
-      float l_tot[G];
+      float l_tot[GS];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
+      for (int g = 0; g < GS; ++g) {
         float x = l_part[g];
 #pragma unroll
         for (int o = 1; o < TPH; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -560,12 +583,12 @@ __global__ void __launch_bounds__(UMMA_THREADS, 1)
       }
       if (t == 0) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          m_sm[h * G + g] = m_run[g];
-          l_sm[h * G + g] = l_tot[g];
+        for (int g = 0; g < GS; ++g) {
+          m_sm[h * G + g0 + g] = m_run[g];
+          l_sm[h * G + g0 + g] = l_tot[g];
         }
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 128 * SW);
       const bool complete = (P == pc.seg_start) && (pc.end == pc.seg_end);
       float *slot = a.partials + (size_t)(2 * blockIdx.x + (pc.seg_start <= rg.b0 ? 0 : 1)) * SLOT;
       if (wait(pvdone, (uint32_t)(gi0 + np - 1) & 1u)) {
@@ -573,7 +596,8 @@ __global__ void __launch_bounds__(UMMA_THREADS, 1)
         const int d = row;
         uint16_t *obase = a.out + ((int64_t)pc.r * a.Hq + (int64_t)pc.hg * HG * G) * D + d;
 #pragma unroll
-        for (int hh = 0; hh < HG; ++hh) {
+        for (int k = 0; k < HG / SW; ++k) {
+          const int hh = hh0 + k;
           uint32_t o[2 * G];
           tmem_ld<2 * G>(tmem_addr(tbase + 2 * N, 32 * qd, hh * 2 * G), o);
 #pragma unroll
@@ -587,7 +611,7 @@ __global__ void __launch_bounds__(UMMA_THREADS, 1)
             }
           }
         }
-        if (!complete && row < HG * G) {
+        if (!complete && set == 0 && row < HG * G) {
           slot[(row / G) * PF + row % G] = m_sm[row];
           slot[(row / G) * PF + G + row % G] = l_sm[row];
         }
@@ -611,7 +635,8 @@ __global__ void __launch_bounds__(UMMA_THREADS, 1)
 template <int G, int S, int QBUF, int DT, int HG, int BPU, bool EARLY>
 static cudaError_t launch_umma_cfg(const DecodeArgs &a, const CUtensorMap &tmK,
                                    const CUtensorMap &tmV, int ctas, cudaStream_t s) {
-  auto kern = decode_umma_kernel<G, S, QBUF, DT, HG, BPU, EARLY>;
+  constexpr int SW = UMMA_SOFTMAX_SETS<G>;
+  auto kern = decode_umma_kernel<G, S, QBUF, DT, HG, BPU, EARLY, SW>;
   const size_t smem = UmmaLayout<G, S, QBUF, HG, BPU>::bytes(a.batch);
   static bool attr_set = false;
   if (!attr_set) {
@@ -620,7 +645,7 @@ static cudaError_t launch_umma_cfg(const DecodeArgs &a, const CUtensorMap &tmK,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  cudaError_t e = launch_pdl(kern, dim3(ctas), dim3(UMMA_THREADS), smem, s, tmK, tmV, a);
+  cudaError_t e = launch_pdl(kern, dim3(ctas), dim3(umma_threads<SW>()), smem, s, tmK, tmV, a);
   if (e != cudaSuccess) return e;
   return launch_combine<128, G, HG, DT, BPU, UMMA_COMBINE_RELEASE_EARLY<EARLY, BPU>>(a, ctas, s);
 }
