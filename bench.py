@@ -613,7 +613,13 @@ def run_gpu(args):
     pf_avg = graph_ms(lambda: eng.prefill(0, pf_q, pf_seq, pf_pos, inp.block_tables, pf_out),
                       reps, use_graph)
     kv_row = cfg.kv_heads * cfg.head_dim * cfg.elem_bytes
-    pf_read = int((pos_h + 1).sum()) * 2 * kv_row
+    # the tensor-core prefill reads, per tile of up to 128 / G consecutive tokens of one
+    # request, K and V of the request's tokens 0 .. the tile's last position once
+    T = 128 // (cfg.q_heads // cfg.kv_heads)
+    tile_last = [int(p[min(t + T, nq) - 1]) for p in pos_h.reshape(cfg.batch, nq)
+                 for t in range(0, nq, T)]
+    pf_read = sum(m + 1 for m in tile_last) * 2 * kv_row
+    pf_qo = 2 * pos_h.size * cfg.q_heads * cfg.head_dim * cfg.elem_bytes  # q in, out
     pf_unique = int(ctx_h.sum()) * 2 * kv_row
     # slot mapping, inject (one launch, or one per layer when overlapped), then per step and
     # layer the append + decode launches
@@ -686,10 +692,13 @@ def run_gpu(args):
     parts.update({
         "prefill": {"query_tokens": int(pos_h.size), "per_request": nq, "layers": 1,
                     "ms": pf_avg, "tokens_per_s": pos_h.size / (pf_avg * 1e-3),
-                    "kv_bytes_read": pf_read, "gbs": pf_read / (pf_avg * 1e-3) / 1e9,
+                    "kv_bytes_read": pf_read, "q_out_bytes": pf_qo,
+                    "gbs": (pf_read + pf_qo) / (pf_avg * 1e-3) / 1e9,
+                    "frac_of_measured": (pf_read + pf_qo) / (pf_avg * 1e-3) / 1e9 / peak,
                     "unique_kv_bytes": pf_unique,
-                    "note": "each query token a decode row over its causal context; "
-                            "unique bytes are each request's context read once"},
+                    "note": "tensor-core tiles of up to 128/G query tokens of one request: "
+                            "K/V of the request's tokens up to the tile's last position read "
+                            "once per tile and kv head; unique bytes = each context once"},
         "copy_blocks": {"blocks": n_copy, "layers": cfg.layers, "bytes": copy_bytes,
                         "ms": copy_avg, "gbs": copy_gbs,
                         "note": "each block copied onto itself: full reads and writes, "

@@ -257,12 +257,23 @@ int kvinj_paged_decode(const kvinj_cache *cache, const kvinj_rope *rope, int32_t
  * softmax(scale * q' . K) V over those tokens of kv head qh / G, q' = q[i][qh]
  * rotated at positions[i] (as given when rope == NULL). q, out: device
  * [n][num_q_heads][D] in the cache dtype; seq_ids, positions: device int32 [n];
- * block_tables: device int32 [batch][max_blocks]. The tokens are computed as
- * decode rows (context positions[i] + 1 under the request's table), in launches
- * of up to 1024 tokens: every row reads its own causal context. workspace:
- * device, kvinj_prefill_workspace_size() bytes, 16-byte aligned, any contents.
- * A request id outside [0, batch) or a position outside the table gives a zero
- * output row, KVINJ_ST_BAD_SEQ or KVINJ_ST_BAD_POS, and KVINJ_ST_BAD_CTX. */
+ * block_tables: device int32 [batch][max_blocks].
+ * At D = 128 and G = num_q_heads / num_kv_heads in {1, 2, 4, 8} the tokens run
+ * on the tensor cores in tiles: up to 128 / G consecutive entries of the token
+ * list that belong to one request share a tile, whose 128 rows are (token,
+ * query head of a kv head's group) pairs, and K and V of the request's tokens
+ * 0 .. (the tile's largest position) are read once per tile and kv head, in
+ * chunks of 128 keys, each row masking the keys after its own position. List
+ * the tokens of a request next to each other: a token whose neighbours belong
+ * to other requests gets a tile of its own. Other shapes run as decode rows
+ * (context positions[i] + 1 under the request's table, launches of up to 1024
+ * tokens: every row reads its own causal context). workspace: device,
+ * kvinj_prefill_workspace_size() bytes, 16-byte aligned, any contents; one call
+ * at a time per workspace. A request id outside [0, batch) or a position
+ * outside the table gives a zero output row, KVINJ_ST_BAD_SEQ or
+ * KVINJ_ST_BAD_POS, and KVINJ_ST_BAD_CTX; a block-table entry outside the cache
+ * is read as a page of masked keys (KVINJ_ST_BAD_BLOCK); a position outside the
+ * RoPE table leaves that query unrotated (KVINJ_ST_BAD_POS). */
 size_t kvinj_prefill_workspace_size(int32_t n, int32_t num_q_heads, int32_t num_kv_heads,
                                     int32_t head_dim, int32_t max_blocks);
 int kvinj_paged_prefill(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,

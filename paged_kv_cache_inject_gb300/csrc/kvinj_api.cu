@@ -472,11 +472,37 @@ int kvinj_append_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rop
 constexpr int PREFILL_CHUNK = 1024;
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+namespace {
+
+// the tensor-core prefill takes D = 128 and G in {1, 2, 4, 8}; other shapes run as decode rows
+bool prefill_umma_ok(int D, int G) { return D == 128 && (G == 1 || G == 2 || G == 4 || G == 8); }
+
+// workspace of the tensor-core prefill: header, tiles, unit prefix, first tile per CTA,
+// partial states
+struct PrefillWs {
+  size_t hdr, tiles, tile_pre, cta_tile, partials, qhl, bytes;
+};
+PrefillWs prefill_umma_ws(int64_t n, int Hq) {
+  const size_t grid = (size_t)num_sms();
+  PrefillWs w;
+  w.hdr = 0;
+  w.tiles = 256;
+  w.tile_pre = w.tiles + align256((size_t)n * 16);
+  w.cta_tile = w.tile_pre + align256(((size_t)n + 1) * 4);
+  w.partials = w.cta_tile + align256(grid * 4);
+  w.qhl = w.partials + align256(2 * grid * prefill_partial_floats() * 4);
+  w.bytes = w.qhl + align256((size_t)n * Hq * 128 * 4);
+  return w;
+}
+
+}  // namespace
+
 size_t kvinj_prefill_workspace_size(int32_t n, int32_t num_q_heads, int32_t num_kv_heads,
                                     int32_t head_dim, int32_t max_blocks) {
   if (n <= 0 || max_blocks <= 0) return 0;
   const size_t dec = kvinj_decode_workspace_size(1, num_q_heads, num_kv_heads, head_dim);
   if (!dec) return 0;
+  if (prefill_umma_ok(head_dim, num_q_heads / num_kv_heads)) return prefill_umma_ws(n, num_q_heads).bytes;
   const size_t rows = (size_t)(n < PREFILL_CHUNK ? n : PREFILL_CHUNK);
   return align256(dec) + align256(rows * max_blocks * 4) + 2 * align256(rows * 4);
 }
@@ -497,6 +523,48 @@ int kvinj_paged_prefill(const kvinj_cache *cache, const kvinj_rope *rope, int32_
                                                    cache->head_dim, max_blocks);
   if (!need) return KVINJ_EINVAL;
   if (ws_bytes < need) return KVINJ_EWORKSPACE;
+  const int D = cache->head_dim, Hkv = cache->num_kv_heads;
+  if (prefill_umma_ok(D, num_q_heads / Hkv)) {
+    if ((rc = check_rope(rope, D))) return rc;
+    if (layer < 0 || layer >= cache->num_layers) return KVINJ_EINVAL;
+    // unit counts and cache rows stay below 2^31
+    if ((int64_t)n * Hkv * ((int64_t)max_blocks * cache->block_size / 128 + 1) >= (int64_t)1 << 31 ||
+        (int64_t)cache->num_layers * cache->num_blocks * Hkv * 16 >= (int64_t)1 << 31)
+      return KVINJ_EUNSUPPORTED;
+    if (!aligned16(q) || !aligned16(out)) return KVINJ_EINVAL;
+    const PrefillWs wl = prefill_umma_ws(n, num_q_heads);
+    char *w = static_cast<char *>(workspace);
+    PrefillArgs p;
+    p.q = static_cast<const uint16_t *>(q);
+    p.seq = seq_ids;
+    p.pos = positions;
+    p.block_tables = block_tables;
+    p.rope = rope ? static_cast<const float4 *>(rope->table) : nullptr;
+    p.max_pos = rope ? rope->max_pos : 0;
+    p.out = static_cast<uint16_t *>(out);
+    p.status = dev_status;
+    p.n = n;
+    p.batch = batch;
+    p.Hq = num_q_heads;
+    p.Hkv = Hkv;
+    p.max_blocks = max_blocks;
+    p.layer = layer;
+    p.num_blocks = cache->num_blocks;
+    const double sc = scale > 0.f ? (double)scale : 1.0 / sqrt((double)D);
+    p.scale_log2 = (float)(sc * 1.4426950408889634);
+    p.grid = num_sms();
+    p.hdr = reinterpret_cast<int *>(w + wl.hdr);
+    p.tiles = reinterpret_cast<int4 *>(w + wl.tiles);
+    p.tile_pre = reinterpret_cast<int *>(w + wl.tile_pre);
+    p.cta_tile = reinterpret_cast<int *>(w + wl.cta_tile);
+    p.partials = reinterpret_cast<float *>(w + wl.partials);
+    p.qhl = reinterpret_cast<uint32_t *>(w + wl.qhl);
+    CUtensorMap tmK, tmV;  // boxes of one head of one block
+    if ((rc = make_cache_map(&tmK, cache->k, cache, 1))) return rc;
+    if ((rc = make_cache_map(&tmV, cache->v, cache, 1))) return rc;
+    return cuda_rc(launch_prefill(p, tmK, tmV, num_q_heads / Hkv, cache->dtype,
+                                  (cudaStream_t)stream));
+  }
   const size_t dec = align256(kvinj_decode_workspace_size(1, num_q_heads, cache->num_kv_heads,
                                                           cache->head_dim));
   const int chunk = n < PREFILL_CHUNK ? n : PREFILL_CHUNK;

@@ -112,6 +112,32 @@ cudaError_t launch_copy_blocks(const CopyBlocksArgs &a, cudaStream_t s);
 
 // paged prefill as decode rows: row i of a chunk is query token i0 + i, with its request's
 // block-table row, context length position + 1 (0 when the token is invalid) and q position
+// paged prefill on the tensor cores (kvinj_prefill.cu): D = 128, G in {1, 2, 4, 8}
+struct PrefillArgs {
+  const uint16_t *q;            // [n][Hq][D]
+  const int32_t *seq, *pos;     // [n]
+  const int32_t *block_tables;  // [batch][max_blocks]
+  const float4 *rope;           // nullptr: q already rotated
+  int max_pos;
+  uint16_t *out;                // [n][Hq][D]
+  int32_t *status;
+  int n, batch, Hq, Hkv, max_blocks, layer;
+  int64_t num_blocks;
+  float scale_log2;             // softmax scale times log2(e)
+  int grid;                     // CTAs of the tensor-core pass
+  // workspace: {tiles, units}; tiles [n] {request, first token, tokens, largest position};
+  // tile_pre [n + 1]; cta_tile [grid]; partial states [2 grid][prefill_partial_floats()];
+  // prepared query rows
+  int *hdr;
+  int4 *tiles;
+  int *tile_pre, *cta_tile;
+  float *partials;
+  uint32_t *qhl;                // [n][Hq][128]: prepared query rows (hi words, then lo)
+};
+size_t prefill_partial_floats();
+cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                           int G, int dtype, cudaStream_t s);
+
 cudaError_t launch_prefill_rows(const int32_t *bt, int max_blocks, int batch, int B,
                                 const int32_t *seq, const int32_t *pos, int64_t i0, int rows,
                                 int32_t *row_bt, int32_t *row_ctx, int32_t *row_qpos,

@@ -130,14 +130,23 @@ def test_prefill_host_validation(lib):
     # no GPU needed: sizes and argument checks happen before any launch
     assert lib.kvinj_prefill_workspace_size(0, 32, 8, 128, 64) == 0
     assert lib.kvinj_prefill_workspace_size(10, 30, 8, 128, 64) == 0  # Hq not a multiple of Hkv
+    r = lambda x: (x + 255) // 256 * 256
+    # tensor-core path (D = 128, G in {1, 2, 4, 8}): a header, 16 bytes of tile and 4 of
+    # unit prefix per query token, per-CTA entries that do not depend on the tokens, and
+    # the prepared query rows (hi and lo 16-bit parts: 512 bytes per query head)
     small = lib.kvinj_prefill_workspace_size(10, 32, 8, 128, 64)
     big = lib.kvinj_prefill_workspace_size(5000, 32, 8, 128, 64)
-    dec = lib.kvinj_decode_workspace_size(1, 32, 8, 128)
-    # the decode's workspace, then the rows' tables, context lengths and q positions
-    # (at most 1024 rows per launch), each 256-byte aligned
-    r = lambda x: (x + 255) // 256 * 256
-    assert small == r(dec) + r(10 * 64 * 4) + 2 * r(10 * 4)
-    assert big == r(dec) + r(1024 * 64 * 4) + 2 * r(1024 * 4)
+    assert small > 0
+    assert big - small == (r(5000 * 16) - r(10 * 16)) + (r(5001 * 4) - r(11 * 4)) + \
+        (r(5000 * 32 * 512) - r(10 * 32 * 512))
+    assert lib.kvinj_prefill_workspace_size(10, 32, 8, 128, 4096) == small  # no table copies
+    # decode rows (other shapes): the decode's workspace, then the rows' tables, context
+    # lengths and q positions (at most 1024 rows per launch), each 256-byte aligned
+    dec = lib.kvinj_decode_workspace_size(1, 8, 4, 64)
+    assert lib.kvinj_prefill_workspace_size(10, 8, 4, 64, 64) == \
+        r(dec) + r(10 * 64 * 4) + 2 * r(10 * 4)
+    assert lib.kvinj_prefill_workspace_size(5000, 8, 4, 64, 64) == \
+        r(dec) + r(1024 * 64 * 4) + 2 * r(1024 * 4)
     cache = K._Cache(2, 8, 128, 16, 10, 0, 0x1000, 0x2000)
     rr = ctypes.byref
     # nothing to do

@@ -694,7 +694,25 @@ def _prefill_case(D, G, dt, mem, nq, Hkv, seed):
     return kc, vc, bt, seq, pos, q
 
 
-def _run_prefill(kc, vc, bt, seq, pos, q, dt, theta, rope_max, status=None):
+def _prefill_grouped(D, G, dt, mem, nq, Hkv, seed, runs=0):
+    # as _prefill_case, with each request's query tokens consecutive in the token list, or
+    # (runs > 0) cut into runs of `runs` tokens, the runs of the requests interleaved
+    ctx = [m + n for m, n in zip(mem, nq)]
+    kc, vc, _, bt = _decode_case(D, G, dt, ctx, Hkv=Hkv, L=2, seed=seed)
+    per = [[(r, mem[r] + i) for i in range(nq[r])] for r in range(len(mem))]
+    if runs:
+        parts = [[p[i:i + runs] for i in range(0, len(p), runs)] for p in per]
+        toks = [t for k in range(max(len(c) for c in parts)) for c in parts if k < len(c)
+                for t in c[k]]
+    else:
+        toks = [t for p in per for t in p]
+    seq = np.array([t[0] for t in toks], np.int32)
+    pos = np.array([t[1] for t in toks], np.int32)
+    q = gen_bits(seed + 9, (len(toks), Hkv * G, D), dt)
+    return kc, vc, bt, seq, pos, q
+
+
+def _run_prefill(kc, vc, bt, seq, pos, q, dt, theta, rope_max, status=None, scale=0.0):
     tdt = torch_dtype(dt)
     D = kc.shape[-1]
     cache = K.Cache(from_bits(kc, tdt), from_bits(vc, tdt))
@@ -703,7 +721,7 @@ def _run_prefill(kc, vc, bt, seq, pos, q, dt, theta, rope_max, status=None):
     ws = K.make_prefill_workspace(n, Hq, kc.shape[2], D, bt.shape[1])
     out = torch.full((n, Hq, D), float("nan"), dtype=tdt, device="cuda")
     K.kvinj_paged_prefill(cache, rope, 1, from_bits(q, tdt), i32(seq), i32(pos), i32(bt), out, ws,
-                          status=status)
+                          scale=scale, status=status)
     torch.cuda.synchronize()
     return out.float().cpu().numpy().astype(np.float64)
 
@@ -740,6 +758,102 @@ def test_paged_prefill_more_tokens_than_a_launch_and_bad_tokens():
                                     n_threads=16)
     assert st == 0
     assert_decode_close(got[keep], want, "prefill over two launches")
+
+
+@pytest.mark.parametrize("dt", [W.BF16, W.FP16])
+@pytest.mark.parametrize("G,Hkv", [(1, 8), (2, 8), (4, 8), (8, 8), (4, 16)])
+def test_paged_prefill_tiles_match_oracle(G, Hkv, dt):
+    # consecutive query tokens of a request share tiles of 128 / G tokens (70 tokens: several
+    # tiles, the last one ragged); contexts up to 4070 tokens stream 32 chunks of 128 keys per
+    # tile and kv head, split over the CTAs (cut segments are merged by the combine pass);
+    # a 1-token request and a 3-token memory
+    D, theta = 128, 5e5
+    mem, nq = [2900, 640, 100, 4000, 3], [40, 17, 5, 70, 1]
+    kc, vc, bt, seq, pos, q = _prefill_grouped(D, G, dt, mem, nq, Hkv, seed=300 + 7 * G + Hkv)
+    status = status_tensor()
+    got = _run_prefill(kc, vc, bt, seq, pos, q, dt, theta, 4200, status=status)
+    assert status.item() == 0
+    want, st = oracle.paged_prefill(kc, vc, 1, q, seq, pos, bt, theta, dt, n_threads=16)
+    assert st == 0
+    assert_decode_close(got, want, f"prefill tiles G{G} Hkv{Hkv} dt{dt}")
+
+
+@pytest.mark.parametrize("scale", [0.5, 2.0])
+def test_paged_prefill_large_logits(scale):
+    # logits 5.7x and 23x the default scale: the running maximum moves within and across
+    # chunks, and the hi + lo parts of q and P carry the precision
+    D, G, Hkv, dt, theta = 128, 8, 8, W.BF16, 5e5
+    mem, nq = [1500, 260], [16, 16]
+    kc, vc, bt, seq, pos, q = _prefill_grouped(D, G, dt, mem, nq, Hkv, seed=330)
+    status = status_tensor()
+    got = _run_prefill(kc, vc, bt, seq, pos, q, dt, theta, 2000, status=status, scale=scale)
+    assert status.item() == 0
+    want, st = oracle.paged_prefill(kc, vc, 1, q, seq, pos, bt, theta, dt, scale=scale,
+                                    n_threads=16)
+    assert st == 0
+    assert_decode_close(got, want, f"prefill scale {scale}")
+
+
+def test_paged_prefill_runs_bad_block_and_determinism():
+    # each request's tokens in runs of 5 interleaved with the others' (tiles never span two
+    # runs); request 1's table points page 10 outside the cache: its rows are flagged, the
+    # other requests' rows are unaffected; a second call gives the same bits
+    D, G, Hkv, dt, theta = 128, 4, 8, W.BF16, 5e5
+    mem, nq = [700, 1200, 300], [33, 21, 12]
+    kc, vc, bt, seq, pos, q = _prefill_grouped(D, G, dt, mem, nq, Hkv, seed=340, runs=5)
+    bt = bt.copy()
+    bt[1, 10] = 10 ** 6
+    status = status_tensor()
+    got = _run_prefill(kc, vc, bt, seq, pos, q, dt, theta, 1600, status=status)
+    assert status.item() == K.ST_BAD_BLOCK
+    keep = seq != 1
+    want, st = oracle.paged_prefill(kc, vc, 1, q[keep], seq[keep], pos[keep], bt, theta, dt,
+                                    n_threads=16)
+    assert st == 0
+    assert_decode_close(got[keep], want, "prefill runs")
+    again = _run_prefill(kc, vc, bt, seq, pos, q, dt, theta, 1600)
+    assert np.array_equal(got, again, equal_nan=True)
+
+
+def test_paged_prefill_ignores_nan_rows_past_the_context():
+    # every cache row that no query token may attend to -- slots past each request's last
+    # token, blocks of no request -- holds NaN bit patterns; request 1's first page of its
+    # second chunk points outside the cache (its copy then comes from block 0, NaN too)
+    D, G, Hkv, dt, theta = 128, 4, 8, W.BF16, 5e5
+    mem, nq = [300, 500, 37], [20, 9, 3]
+    kc, vc, bt, seq, pos, q = _prefill_grouped(D, G, dt, mem, nq, Hkv, seed=360)
+    ctx = np.array([m + n for m, n in zip(mem, nq)])
+    used = np.zeros(kc.shape[1:3] + (16,), bool)[:, 0]  # [NB][16] slots holding a token
+    for r, c in enumerate(ctx):
+        for t in range(c):
+            used[bt[r, t // 16], t % 16] = True
+    nan = 0x7FC0
+    kc, vc = kc.copy(), vc.copy()
+    nb, slot = np.nonzero(~used)
+    kc[:, nb, :, slot, :] = nan
+    vc[:, nb, :, slot, :] = nan
+    bad = bt.copy()
+    bad[1, 8] = -5
+    status = status_tensor()
+    got = _run_prefill(kc, vc, bad, seq, pos, q, dt, theta, 600, status=status)
+    assert status.item() == K.ST_BAD_BLOCK
+    assert np.isfinite(got).all()
+    keep = seq != 1
+    want, st = oracle.paged_prefill(kc, vc, 1, q[keep], seq[keep], pos[keep], bt, theta, dt,
+                                    n_threads=16)
+    assert st == 0
+    assert_decode_close(got[keep], want, "prefill with NaN rows outside the contexts")
+
+
+def test_paged_prefill_all_tokens_invalid():
+    # no valid token: every row zero, no tile, no unit; the tensor-core pass does nothing
+    D, G, Hkv, dt, theta = 128, 4, 8, W.BF16, 5e5
+    kc, vc, bt, seq, pos, q = _prefill_grouped(D, G, dt, [50, 20], [3, 2], Hkv, seed=350)
+    seq = np.array([5, -1, 2, 9, 7], np.int32)
+    status = status_tensor()
+    got = _run_prefill(kc, vc, bt, seq, pos, q, dt, theta, 100, status=status)
+    assert status.item() & K.ST_BAD_SEQ
+    assert not got.any()
 
 
 # ---------------------------------------------------------------------------
