@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(umma_threads<SW>(), 1)
             m_run[g] = mu;
             resc = true;
           }
-          p[g] = (s[g] == -INFINITY) ? 0.f : exp2f(s[g] - m_run[g]);
+          p[g] = (s[g] == -INFINITY) ? 0.f : ex2_approx(s[g] - m_run[g]);
           l_part[g] = __fmaf_rn(l_part[g], alpha[g], p[g]);
         }
         if (t == 0) {

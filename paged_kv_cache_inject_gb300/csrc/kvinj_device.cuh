@@ -45,6 +45,15 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {  // round to neare
   }
 }
 
+// 2^x by the special-function unit's approximation (ex2.approx.ftz: relative error near
+// 2^-22; 2^-inf = +0). The softmax kernels call it with x <= their lazy-maximum threshold;
+// it is several times cheaper per element here than exp2f.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------------------
 // RoPE rotation of one pair (a = x_i, b = x_{i+D/2}) by the angle whose cos
 // and sin are c = t.x + t.z and s = t.y + t.w (hi + lo parts of the fp64

@@ -112,14 +112,6 @@ __device__ __forceinline__ void tmem_st16_nw(uint32_t taddr, const uint32_t (&r)
                : "memory");
 }
 
-// 2^x by the special-function unit's approximation (relative error near 2^-22); x is at
-// most 8 here, -inf for masked keys (2^-inf = +0)
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // D[tmem] (+)= A[tmem] * B[smem], issued by one thread; acc = 0 overwrites D
 __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                 uint32_t idesc, uint32_t acc) {
