@@ -155,13 +155,33 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# the sources each profiled kernel's counters depend on: its own files, plus the shared
+# device headers and the launch path
+_KERNEL_SOURCES = {
+    "decode_i8": ["kvinj_decode_i8.cu", "kvinj_decode_common.cuh"],
+    "decode": ["kvinj_decode_umma.cuh", "kvinj_decode_umma.cu", "kvinj_decode_umma_early.cu",
+               "kvinj_decode_common.cuh"],
+    "inject_i8": ["kvinj_inject_i8.cu"],
+    "inject": ["kvinj_inject.cu"],
+    "copy_blocks": ["kvinj_inject.cu"],
+    "prefill": ["kvinj_prefill.cu"],
+}
+_COMMON_SOURCES = ["kvinj_device.cuh", "kvinj_umma.cuh", "kvinj_internal.h", "kvinj_api.cu"]
+
+
+def _kernel_kind(tag: str) -> str:
+    # the longest kind the tag starts with ("decode_i8_..." before "decode_...")
+    kinds = [k for k in _KERNEL_SOURCES if tag.startswith(k + "_")]
+    return max(kinds, key=len) if kinds else ""
+
+
 def _traffic_from_profile(kernel_tag: str):
     """dram bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source (the summary records the source hash)."""
+    the current source of that kernel (the summary records the hash)."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}.txt")
     if not os.path.exists(path):
         return None
-    src = _source_hash()
+    src = _source_hash(_kernel_kind(kernel_tag))
     want_hash, value = None, None
     for ln in open(path):
         if ln.startswith("source_sha256:"):
@@ -174,12 +194,17 @@ def _traffic_from_profile(kernel_tag: str):
     return value if want_hash == src else None
 
 
-def _source_hash() -> str:
-    h = hashlib.sha256()
+def _source_hash(kind: str = "") -> str:
+    """sha256 (16 hex digits) of the sources of one kernel kind (every file under csrc/
+    for an unknown kind)."""
     csrc = os.path.join(ROOT, "paged_kv_cache_inject_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    if kind in _KERNEL_SOURCES:
+        names = sorted(set(_KERNEL_SOURCES[kind] + _COMMON_SOURCES))
+    else:
+        names = sorted(n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h")))
+    h = hashlib.sha256()
+    for name in names:
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -696,6 +721,7 @@ def run_gpu(args):
                     "gbs": (pf_read + pf_qo) / (pf_avg * 1e-3) / 1e9,
                     "frac_of_measured": (pf_read + pf_qo) / (pf_avg * 1e-3) / 1e9 / peak,
                     "unique_kv_bytes": pf_unique,
+                    "traffic": _traffic_from_profile(f"prefill_{cfg.name}"),
                     "note": "tensor-core tiles of up to 128/G query tokens of one request: "
                             "K/V of the request's tokens up to the tile's last position read "
                             "once per tile and kv head; unique bytes = each context once"},
