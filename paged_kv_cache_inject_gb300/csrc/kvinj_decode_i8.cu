@@ -35,12 +35,14 @@
 // The fused append writes the new token's codes and scales (rotated exactly,
 // then quantized, as the int8 inject does) before its block is streamed.
 //
-// Warp roles (384 threads):
+// Warp roles (384 threads, 512 with two softmax sets at G >= 2):
 //   warp 0      TMA producer (int8 stages)
 //   warp 1      TMEM owner; lane 0 issues every MMA and commit
 //   warps 2-3   query preparation and the fused append
-//   warps 4-7   softmax, P tile, rescaling of O, end-of-piece output
+//   warps 4-7   softmax, P tile, rescaling of O, end-of-piece output (set 0)
 //   warps 8-11  converters (warp 8 + i owns unit rows 32i .. 32i + 31)
+//   warps 12-15 softmax set 1 at G >= 2: the same rows as set 0, the other half of each kv
+//               head's query heads (and of O's columns)
 // Every wait is bounded; a wait that gives up sets the abort flag and
 // KVINJ_ST_TIMEOUT, and all roles still reach the final barrier.
 #include <math.h>
@@ -53,7 +55,13 @@ namespace kvinj {
 namespace {
 
 constexpr float I8_TAU = 8.f;  // lazy-maximum threshold, log2 units
-constexpr int I8_THREADS = 384;
+// threads: 0 producer, 1 MMA, 2-3 queries, 4-7 softmax set 0, 8-11 converters, and with
+// two softmax sets (G >= 2) 12-15 set 1 (the same tensor-memory lanes as set 0; each set owns
+// half of the query heads of every kv head)
+template <int SW>
+constexpr int i8_threads() { return 256 + 128 * SW; }
+template <int G>
+constexpr int I8_SOFTMAX_SETS = G >= 2 ? 2 : 1;
 
 template <int G_, int S_, int QBUF_, int HG_, int BPU_>
 struct I8Layout {
@@ -90,9 +98,9 @@ struct I8Layout {
   static constexpr int off_qfull = off_xbar + 6 * 8;
   static constexpr int off_valid = off_xbar + NXBAR * 8;   // [VR] valid bits
   static constexpr int off_qinfo = off_valid + VR * 4;     // unused (no bytes)
-  static constexpr int off_flags = off_qinfo;              // [0] abort [8..20) scan
-  static constexpr int off_alpha = off_flags + 96;         // [2][N] factors, [2][4] flags
-  static constexpr int off_ml = off_alpha + 2 * N * 4 + 32;
+  static constexpr int off_flags = off_qinfo;              // [0] abort [8..24) scan
+  static constexpr int off_alpha = off_flags + 96;         // [2][N] factors, [2][8] flags
+  static constexpr int off_ml = off_alpha + 2 * N * 4 + 64;
   static constexpr int off_tmem = off_ml + 2 * HG * G * 4;
   static constexpr int off_pre = off_tmem + 16;            // pre[batch + 1], then qpos[batch]
   // tensor memory: S[2] at columns 0 and N, O at 2N, the K operands [2] at KT and KT + 64,
@@ -188,8 +196,8 @@ __device__ __forceinline__ float val16(uint16_t b) {
   else return __half2float(__ushort_as_half(b));
 }
 
-template <int G, int S, int QBUF, int DT, int HG, int BPU>
-__global__ void __launch_bounds__(I8_THREADS, 1)
+template <int G, int S, int QBUF, int DT, int HG, int BPU, int SW>
+__global__ void __launch_bounds__(i8_threads<SW>(), 1)
     decode_i8_kernel(const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, DecodeArgs a) {
   using Lay = I8Layout<G, S, QBUF, HG, BPU>;
@@ -200,6 +208,9 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
   constexpr int TPH = BLK * BPU;   // tokens of a head in a unit (its rows are consecutive)
   constexpr int HPW = 32 / TPH;    // heads per softmax warp
   static_assert(G == 1 || G == 2 || G == 4 || G == 8, "int8 decode: G");
+  constexpr int NT = i8_threads<SW>();
+  constexpr int GS = G / SW;       // query heads per kv head of one softmax set
+  static_assert(SW == 1 || (SW == 2 && G >= 2 && HG % 2 == 0), "softmax sets");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = smem_raw;
@@ -219,16 +230,16 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(sfull + b, 1);
-      mbar_init(sfree + b, 4);
+      mbar_init(sfree + b, 4 * SW);
       mbar_init(kfull + b, 4);
     }
-    mbar_init(pfull, 4);
+    mbar_init(pfull, 4 * SW);
     mbar_init(pvdone, 1);
     for (int b = 0; b < QBUF; ++b) {
       mbar_init(qfull + b, 2);
       mbar_init(qempty + b, 1);
     }
-    mbar_init(ofree, 4);
+    mbar_init(ofree, 4 * SW);
     mbar_init(done, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(vfull + b, 4);
@@ -241,7 +252,7 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
     tmem_relinquish();
   }
   CtaRange rg;
-  const bool has_units = decode_prologue<Lay, I8_THREADS>(a, sm, rg);
+  const bool has_units = decode_prologue<Lay, NT>(a, sm, rg);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -430,25 +441,28 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
       P = pc.end;
       ++piece;
     }
-  } else if (warp < 8) {
+  } else if (warp < 8 || warp >= 12) {
     // -------------------------------- softmax --------------------------------
     const int qd = warp & 3;
+    const int set = SW == 1 ? 0 : (warp >= 12 ? 1 : 0);  // query heads g0 .. g0 + GS - 1
+    const int g0 = set * GS, hh0 = set * (HG / SW);     // ... and this set's O columns
     const int row = 32 * qd + lane;  // unit row = head * TPH + token; O row = dimension
     const int hs = lane / TPH, h = HPW * qd + hs, t = lane % TPH;
     float *alpha_sm = reinterpret_cast<float *>(sm + Lay::off_alpha);
     volatile int *rflag = reinterpret_cast<volatile int *>(alpha_sm + 2 * N);
     float *m_sm = reinterpret_cast<float *>(sm + Lay::off_ml), *l_sm = m_sm + HG * G;
     // the P tile's off-diagonal blocks stay zero
-    for (int i = tid - 128; i < Lay::TILE_BYTES / 16; i += 128) sts128z_(p0 + 16 * i);
+    for (int i = 128 * set + 32 * qd + lane; i < Lay::TILE_BYTES / 16; i += 128 * SW)
+      sts128z_(p0 + 16 * i);
     fence_async_smem();
 
     int P = rg.b0, gi0 = 0;
     while (P < rg.b1) {
       const Piece pc = find_piece<BPU>(a, pre, ngrp, P, rg.b1);
       const int np = pc.end - P;
-      float m_run[G], l_part[G];
+      float m_run[GS], l_part[GS];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
+      for (int g = 0; g < GS; ++g) {
         m_run[g] = -INFINITY;
         l_part[g] = 0.f;
       }
@@ -456,7 +470,7 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
         const int gi = gi0 + j, par = gi & 1;
         const bool ok = wait(sfull + par, (uint32_t)(gi >> 1) & 1u);
         const int tok = (pc.pg0 + j) * TPH + t;
-        float s[G], sk = 0.f, sv = 0.f;
+        float s[GS], sk = 0.f, sv = 0.f;
         uint32_t vflag = 0;
         if (ok) {
           tc_fence_after();
@@ -467,22 +481,25 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
           sk = __uint_as_float(q4[0]);
           sv = __uint_as_float(q4[1]);
           vflag = q4[2];
-#pragma unroll
-          for (int g = 0; g < G; ++g)
-            s[g] = (HPW == 2 && hs) ? __uint_as_float(r[(2 * G + g) % (HPW * 2 * G)]) +
+          // (register indices stay compile-time: a set picks its half by a select)
+          auto score = [&](int g) {
+            return (HPW == 2 && hs) ? __uint_as_float(r[(2 * G + g) % (HPW * 2 * G)]) +
                                           __uint_as_float(r[(3 * G + g) % (HPW * 2 * G)])
                                     : __uint_as_float(r[g]) + __uint_as_float(r[G + g]);
+          };
+#pragma unroll
+          for (int gl = 0; gl < GS; ++gl) s[gl] = (SW == 2 && set) ? score(GS + gl) : score(gl);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(sfree + par);
         const bool live = ok && vflag && tok < pc.ctx && tok >= pc.lo;
 #pragma unroll
-        for (int g = 0; g < G; ++g) s[g] = live ? s[g] * sk : -INFINITY;
-        float alpha[G], p[G];
+        for (int g = 0; g < GS; ++g) s[g] = live ? s[g] * sk : -INFINITY;
+        float alpha[GS], p[GS];
         bool resc = false;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int g = 0; g < GS; ++g) {
           float mu = s[g];
 #pragma unroll
           for (int o = 1; o < TPH; o <<= 1) mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, o));
@@ -492,21 +509,23 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
             m_run[g] = mu;
             resc = true;
           }
-          p[g] = (s[g] == -INFINITY) ? 0.f : exp2f(s[g] - m_run[g]);
+          p[g] = (s[g] == -INFINITY) ? 0.f : ex2_approx(s[g] - m_run[g]);
           l_part[g] = __fmaf_rn(l_part[g], alpha[g], p[g]);
         }
         if (t == 0) {
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            alpha_sm[par * N + h * 2 * G + g] = alpha[g];
-            alpha_sm[par * N + h * 2 * G + G + g] = alpha[g];
+          for (int g = 0; g < GS; ++g) {
+            alpha_sm[par * N + h * 2 * G + g0 + g] = alpha[g];
+            alpha_sm[par * N + h * 2 * G + G + g0 + g] = alpha[g];
           }
         }
         const int any = __any_sync(0xffffffffu, resc);
-        if (lane == 0) rflag[par * 4 + qd] = any;
-        named_bar_sync(1, 128);
-        const bool need =
-            j > 0 && (rflag[par * 4] | rflag[par * 4 + 1] | rflag[par * 4 + 2] | rflag[par * 4 + 3]);
+        if (lane == 0) rflag[par * 8 + set * 4 + qd] = any;
+        named_bar_sync(1, 128 * SW);
+        int anyr = 0;
+#pragma unroll
+        for (int f = 0; f < 4 * SW; ++f) anyr |= rflag[par * 8 + f];
+        const bool need = j > 0 && anyr;
         // PV of the previous unit done: the P tile is free and O is current
         bool okpv = true;
         if (j > 0) {
@@ -515,7 +534,8 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
         }
         if (need && okpv) {
 #pragma unroll
-          for (int hh = 0; hh < HG; ++hh) {
+          for (int k = 0; k < HG / SW; ++k) {
+            const int hh = hh0 + k;
             uint32_t o[2 * G];
             const uint32_t ta = tmem_addr(tbase + 2 * N, 32 * qd, hh * 2 * G);
             tmem_ld<2 * G>(ta, o);
@@ -527,8 +547,9 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
         }
         // P^T: column k = row of this thread; each probability times its row's V scale
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float pv = live ? p[g] * sv : 0.f;
+        for (int gl = 0; gl < GS; ++gl) {
+          const int g = g0 + gl;
+          const float pv = live ? p[gl] * sv : 0.f;
           const uint16_t hi = f32_to16<OT>(pv);
           const uint16_t lo = f32_to16<OT>(pv - val16<OT>(hi));
           sts16_(p0 + i8_tile_off<N>(h * 2 * G + g, row), hi);
@@ -541,9 +562,9 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
       }
 
       // ---- end of piece: outputs or the partial state ----
-      float l_tot[G];
+      float l_tot[GS];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
+      for (int g = 0; g < GS; ++g) {
         float x = l_part[g];
 #pragma unroll
         for (int o = 1; o < TPH; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -551,12 +572,12 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
       }
       if (t == 0) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          m_sm[h * G + g] = m_run[g];
-          l_sm[h * G + g] = l_tot[g];
+        for (int g = 0; g < GS; ++g) {
+          m_sm[h * G + g0 + g] = m_run[g];
+          l_sm[h * G + g0 + g] = l_tot[g];
         }
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 128 * SW);
       const bool complete = (P == pc.seg_start) && (pc.end == pc.seg_end);
       float *slot = a.partials + (size_t)(2 * blockIdx.x + (pc.seg_start <= rg.b0 ? 0 : 1)) * SLOT;
       if (wait(pvdone, (uint32_t)(gi0 + np - 1) & 1u)) {
@@ -564,7 +585,8 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
         const int d = row;
         uint16_t *obase = a.out + ((int64_t)pc.r * a.Hq + (int64_t)pc.hg * HG * G) * D + d;
 #pragma unroll
-        for (int hh = 0; hh < HG; ++hh) {
+        for (int k = 0; k < HG / SW; ++k) {
+          const int hh = hh0 + k;
           uint32_t o[2 * G];
           tmem_ld<2 * G>(tmem_addr(tbase + 2 * N, 32 * qd, hh * 2 * G), o);
 #pragma unroll
@@ -578,7 +600,7 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
             }
           }
         }
-        if (!complete && row < HG * G) {
+        if (!complete && set == 0 && row < HG * G) {
           slot[(row / G) * PF + row % G] = m_sm[row];
           slot[(row / G) * PF + G + row % G] = l_sm[row];
         }
@@ -677,7 +699,8 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
 template <int G, int S, int QBUF, int DT, int HG, int BPU>
 cudaError_t launch_i8_cfg(const DecodeArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmV,
                           int ctas, cudaStream_t s) {
-  auto kern = decode_i8_kernel<G, S, QBUF, DT, HG, BPU>;
+  constexpr int SW = I8_SOFTMAX_SETS<G>;
+  auto kern = decode_i8_kernel<G, S, QBUF, DT, HG, BPU, SW>;
   const size_t smem = I8Layout<G, S, QBUF, HG, BPU>::bytes(a.batch);
   static bool attr_set = false;
   if (!attr_set) {
@@ -686,7 +709,7 @@ cudaError_t launch_i8_cfg(const DecodeArgs &a, const CUtensorMap &tmK, const CUt
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  cudaError_t e = launch_pdl(kern, dim3(ctas), dim3(I8_THREADS), smem, s, tmK, tmV, a);
+  cudaError_t e = launch_pdl(kern, dim3(ctas), dim3(i8_threads<SW>()), smem, s, tmK, tmV, a);
   if (e != cudaSuccess) return e;
   return launch_combine<128, G, HG, DT, BPU>(a, ctas, s);
 }
