@@ -29,15 +29,20 @@
 //   warp 1     tensor-memory owner and MMA issuer, per unit
 //                S  = Q K^T  (A = Q hi, lo from tensor memory, B = K, K-major)
 //                O += P V    (A = P hi, lo from tensor memory, B = V, MN-major)
-//   warps 4-7  softmax, one row per thread (tensor-memory lanes 32 (warp % 4)
-//              onward): the row of S masked (keys after the row's position, or
-//              in a page outside the cache), a lazy running maximum, P = 2^(S -
-//              m) split into hi + lo 16-bit parts written over S's columns, O's
-//              row rescaled when the maximum moved; at the end of a piece O / l
-//              to the output, or (m, l, O) to the workspace
-//   warps 8-11 the prepared query rows of the next piece into tensor memory,
-//              once the current piece's last S is computed
-// Tensor memory (512 columns): S[2] at 0 and 128 (P over them), O at 256,
+//   warps 4-11 softmax in two sets on the same rows, one row per thread
+//              (tensor-memory lanes 32 (warp % 4) onward): set 0 (warps 4-7)
+//              keys 0-63 of each chunk and O columns 0-63, set 1 (warps 8-11)
+//              keys 64-127 and O columns 64-127. Per unit: this set's part of
+//              the row of S masked (keys after the row's position, or in a page
+//              outside the cache), the rows' maxima exchanged, a lazy running
+//              maximum, P = 2^(S - m) split into hi + lo 16-bit parts written
+//              over the set's own columns of S, O rescaled when the maximum
+//              moved; at the end
+//              of a piece O / l to the output, or (m, l, O) to the workspace,
+//              and the next piece's prepared query rows into tensor memory
+//              (set 0 the hi parts, set 1 the lo parts)
+// Tensor memory (512 columns): S[2] at 0 and 128 (P over them: keys 64k ..
+// 64k + 63 as hi words at 64k + j, lo words at 64k + 32 + j), O at 256,
 // Q hi at 384, Q lo at 448. Every wait is bounded and reports
 // KVINJ_ST_TIMEOUT when it gives up.
 #include "kvinj_device.cuh"
@@ -52,11 +57,11 @@ constexpr int PF_D = 128;
 constexpr int BLK = 16;                   // tokens per page
 constexpr int PF_S = 3;                   // stages
 constexpr int PF_THREADS = 384;           // 12 warps = 3 warpgroups
-// registers per thread of each warpgroup after setmaxnreg (warps 0-3: 168 -> 120, softmax:
-// 168 -> 224, query rows: 168 -> 160): the launch provides 384 x 168 = 64512, and
-// 128 x (120 + 224 + 160) = 64512 -- the softmax's increase is exactly what the others free
-constexpr int PF_REG_LAUNCH = 168, PF_REG_CTRL = 120, PF_REG_SOFTMAX = 224, PF_REG_QUERY = 160;
-static_assert(128 * (PF_REG_CTRL + PF_REG_SOFTMAX + PF_REG_QUERY) <= PF_THREADS * PF_REG_LAUNCH,
+// registers per thread of each warpgroup after setmaxnreg (warps 0-3: 168 -> 120, each
+// softmax set: 168 -> 192): the launch provides 384 x 168 = 64512, and 128 x (120 + 2 x 192)
+// = 64512 -- the softmax sets' increase is exactly what the first warpgroup frees
+constexpr int PF_REG_LAUNCH = 168, PF_REG_CTRL = 120, PF_REG_SOFTMAX = 192;
+static_assert(128 * (PF_REG_CTRL + 2 * PF_REG_SOFTMAX) <= PF_THREADS * PF_REG_LAUNCH,
               "prefill: register split");
 constexpr int PF_TB = 1024;               // threads of the tile builder
 constexpr int PF_SLOT = 128 * (PF_D + 2); // floats of a partial state: m[128] l[128] O[D][128]
@@ -75,7 +80,9 @@ struct PfLayout {
   static constexpr int off_valid = off_bar + NBAR * 8;  // [S] page bits of each stage
   static constexpr int off_flags = off_valid + PF_S * 4;  // [0] abort
   static constexpr int off_tmem = off_flags + 16;
-  static constexpr int bytes = off_tmem + 16;
+  // the softmax sets' exchange: rows' maxima [2 parities][2 sets][128], sums [2 sets][128]
+  static constexpr int off_mx = (off_tmem + 16 + 15) / 16 * 16;
+  static constexpr int bytes = off_mx + (4 * 128 + 2 * 128) * 4;
 };
 static_assert(PfLayout::bytes <= 227 * 1024, "prefill: shared memory");
 
@@ -91,17 +98,6 @@ __device__ __forceinline__ void regs_inc() {
 
 __device__ __forceinline__ void sts128_zero(uint32_t addr) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
-}
-
-// one row of 128 columns of tensor memory (32x32b shape, lane = this thread's row), the
-// wait in the same statement so that no use of the registers can precede it
-__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
-      : "r"(taddr)
-      : "memory");
 }
 
 // 32x32b.x16 store that does not wait for its completion (tmem_wait_st does)
@@ -346,11 +342,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       mbar_init(full + s, 1);   // the producer's arrive + the copies' bytes
       mbar_init(empty + s, 1);  // the MMA's commit after the unit's PV
     }
-    mbar_init(tq, 4);     // the query warps: Q of a piece in tensor memory
+    mbar_init(tq, 8);     // the softmax warps: Q of a piece in tensor memory
     mbar_init(qfree, 1);  // the MMA's commit after a piece's last QK
     for (int b = 0; b < 2; ++b) {
       mbar_init(sfull + b, 1);
-      mbar_init(pfull + b, 4);  // the softmax warps: P in tensor memory, O rescaled
+      mbar_init(pfull + b, 8);  // the softmax warps: P in tensor memory, O rescaled
     }
     mbar_init(pvdone, 1);
     mbar_init(done, 1);
@@ -456,9 +452,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const uint32_t pa = tbase + TM_S + (g & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
+          // keys 16 kk .. 16 kk + 15: softmax set kk / 4 wrote their P hi words at
+          // 64 (kk / 4) + 8 (kk % 4) and lo words 32 columns further
+          const uint32_t ph = pa + 64 * (kk >> 2) + 8 * (kk & 3);
           const uint64_t bd = umma_desc_sw128(vb + kk * 2048, Lay::BOX, 1024);
-          umma_f16_tmem_a(tbase + TM_O, pa + kk * 8, bd, ID_PV, (first && kk == 0) ? 0u : 1u);
-          umma_f16_tmem_a(tbase + TM_O, pa + 64 + kk * 8, bd, ID_PV, 1u);
+          umma_f16_tmem_a(tbase + TM_O, ph, bd, ID_PV, (first && kk == 0) ? 0u : 1u);
+          umma_f16_tmem_a(tbase + TM_O, ph + 32, bd, ID_PV, 1u);
         }
         umma_commit(empty + g % PF_S);
         umma_commit(pvdone);
@@ -507,14 +506,58 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     __syncwarp();
   } else if (warp < 4) {
     // warps 2-3: no role
-  } else if (warp < 8) {
+  } else {
     // -------------------------------- softmax --------------------------------
+    // two sets on the same rows: set 0 (warps 4-7) keys 0-63 of each chunk and O columns
+    // 0-63, set 1 (warps 8-11) keys 64-127 and O columns 64-127; they exchange the rows'
+    // maxima per unit and their sums per piece. Each set also copies its half of the next
+    // piece's prepared query rows (set 0 the hi words, set 1 the lo words).
     regs_inc<PF_REG_SOFTMAX>();
+    const int set = warp >= 8 ? 1 : 0;
     const int qd = warp & 3;
     const int m = 32 * qd + lane;  // tile row = tensor-memory lane
     const int tr = m / G, g = m % G;
-    int gi = 0;
-    for (int u = b0; u < b1;) {
+    float *mxb = reinterpret_cast<float *>(sm + Lay::off_mx);  // [2 parities][2 sets][128]
+    float *lxb = mxb + 4 * 128;                                 // [2 sets][128]
+    // the prepared query row of this thread in a piece: 16 words-quads (its set's half)
+    auto q_src = [&](const PfWalk &wk, const PfPiece &pq) {
+      const bool r_ok = tr < wk.t.z;
+      const int64_t row = (int64_t)(r_ok ? wk.t.y + tr : 0) * a.Hq + (int64_t)pq.h * G + g;
+      return r_ok ? reinterpret_cast<const uint4 *>(a.qhl + row * PF_D) + 16 * set : nullptr;
+    };
+    auto q_store = [&](const uint4 (&v)[16]) {
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t wv[16];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          wv[4 * e] = v[4 * q4 + e].x;
+          wv[4 * e + 1] = v[4 * q4 + e].y;
+          wv[4 * e + 2] = v[4 * q4 + e].z;
+          wv[4 * e + 3] = v[4 * q4 + e].w;
+        }
+        tmem_st16_nw(tmem_addr(tbase, 32 * qd, (set ? TM_QLO : TM_QHI) + 16 * q4), wv);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tq);
+    };
+    // Every thread of both sets runs the same sequence of named barriers whatever happens: a
+    // wait that gave up (the abort flag; later waits return at once) only skips work.
+    int gi = 0, piece = 0;
+    bool ok = true;
+    {
+      // the first piece's query rows
+      w.seek(a, b0);
+      const PfPiece pq = pf_piece(w, b0, b1);
+      const uint4 *src = q_src(w, pq);
+      uint4 v[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = src ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
+      q_store(v);
+    }
+    for (int u = b0; u < b1; ++piece) {
       w.seek(a, u);
       const PfPiece pc = pf_piece(w, u, b1);
       const int i0 = w.t.y, nt = w.t.z, mp = w.t.w;
@@ -523,86 +566,101 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       const int p = rv ? __ldg(a.pos + tok) : -1;
       const bool wlive = __any_sync(0xffffffffu, rv);
       float m_run = -INFINITY, l_run = 0.f;
-      bool ok = true;
       for (int j = 0, c = pc.c0; u < pc.u1; ++u, ++j, ++c, ++gi) {
         const int st = gi % PF_S, par = gi & 1;
-        ok = wait(full + st, (uint32_t)(gi / PF_S) & 1u) &&
+        ok = ok && wait(full + st, (uint32_t)(gi / PF_S) & 1u) &&
              wait(sfull + par, (uint32_t)(gi >> 1) & 1u);
-        if (!ok) break;
+        ok = __all_sync(0xffffffffu, ok);  // it gates warp-wide tensor-memory operations
+        const bool work = ok && wlive;
         tc_fence_after();
-        // mask: keys after the row's position, pages outside the cache, empty rows
         const int vb = valid[st];
-        const int lim = p - c * 128;  // keys 0 .. lim of the chunk are attended to
+        // this set's keys 64 set + e, e < 64, are attended to when at or before the row's
+        // position and in a page in the cache
+        const int lim = p - c * 128 - 64 * set;
         const uint32_t ts = tmem_addr(tbase, 32 * qd, TM_S + par * 128);
-        float alpha = 1.f;
-        bool resc = false;
+        float mu_own = -INFINITY;
+        uint32_t mw[2] = {0u, 0u};
         // a warp whose rows hold no token (a tile of fewer than 128 / G tokens) skips the
         // math (tensor-memory loads and stores are warp-wide): its P and O rows are never
         // read out, and an O row depends on its own P row only
-        if (wlive) {
-        // bit e of mw[e / 32]: key e is attended to (e <= lim, its page in the cache)
-        uint32_t mw[4];
+        if (work) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int nk = min(max(lim - 32 * q + 1, 0), 32);
-          const uint32_t keys = nk >= 32 ? 0xFFFFFFFFu : ((1u << nk) - 1u);
-          const uint32_t pages = (((vb >> (2 * q)) & 1) ? 0x0000FFFFu : 0u) |
-                                 (((vb >> (2 * q + 1)) & 1) ? 0xFFFF0000u : 0u);
-          mw[q] = keys & pages;
+          for (int q = 0; q < 2; ++q) {
+            const int nk = min(max(lim - 32 * q + 1, 0), 32);
+            const uint32_t keys = nk >= 32 ? 0xFFFFFFFFu : ((1u << nk) - 1u);
+            const int pg = 4 * set + 2 * q;  // pages of keys 32 q .. 32 q + 31 of this set
+            const uint32_t pages = (((vb >> pg) & 1) ? 0x0000FFFFu : 0u) |
+                                   (((vb >> (pg + 1)) & 1) ? 0xFFFF0000u : 0u);
+            mw[q] = keys & pages;
+          }
+          // this set's 64 columns of S, 32 at a time (read again below for P)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t x[32];
+            tmem_ld<32>(ts + 64 * set + 32 * q, x);
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if ((mw[q] >> e) & 1u) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(x[e]));
+            mu_own = fmaxf(mu_own, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])));
+          }
         }
-        const bool all = (mw[0] & mw[1] & mw[2] & mw[3]) == 0xFFFFFFFFu;
-        // the row of S, masked keys set to -inf
-        uint32_t x[128];
-        tmem_ld128(ts, x);
-        if (!all) {
-#pragma unroll
-          for (int e = 0; e < 128; ++e)
-            if (!((mw[e >> 5] >> (e & 31)) & 1u)) x[e] = __float_as_uint(-INFINITY);
-        }
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int e = 0; e < 128; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(x[e]));
-        const float mu = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        // the row's maximum over both sets' keys
+        mxb[(par * 2 + set) * 128 + m] = mu_own;
+        named_bar_sync(1, 256);
+        const float mu = fmaxf(mu_own, mxb[(par * 2 + (set ^ 1)) * 128 + m]);
+        float alpha = 1.f;
+        bool resc = false;
         if (mu > m_run + 8.f) {  // lazy maximum (also the first finite one)
           alpha = exp2f(m_run - mu);
           m_run = mu;
           resc = true;
         }
-        // P = 2^(S - m) <= 2^8 (0 for masked keys), hi + lo 16-bit parts: hi over S's
-        // columns 0-63, lo over 64-127 (key k at column k / 2)
-        // masked keys are -inf: 2^-inf = +0 (a row with no key yet subtracts 0, not -inf)
-        const float mr = m_run == -INFINITY ? 0.f : m_run;
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        float sum = 0.f;
+        if (work) {
+          // P = 2^(S - m) <= 2^8 (0 for masked keys), hi + lo 16-bit parts, over this set's
+          // own 64 columns of S: hi words (keys 2j, 2j + 1 of the set) at 64 set + j, lo
+          // words at 64 set + 32 + j. The lo words of keys 0-31 wait until keys 32-63 are
+          // read (their columns hold S of keys 32-63).
+          float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+          uint32_t lo[2][16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          // keys 32 q .. 32 q + 31 (all of S is in registers: any order of stores is safe)
-          uint32_t hi[16], lo[16];
+          for (int q = 0; q < 2; ++q) {
+            uint32_t x[32], hi[16];
+            tmem_ld<32>(ts + 64 * set + 32 * q, x);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float s0 = __uint_as_float(x[32 * q + 2 * e]);
-            const float s1 = __uint_as_float(x[32 * q + 2 * e + 1]);
-            const float p0 = ex2_approx(s0 - mr), p1 = ex2_approx(s1 - mr);
-            sum4[e & 3] += p0 + p1;
-            hi[e] = pack2<DT>(p0, p1);
-            const float2 h = unpack2<DT>(hi[e]);
-            lo[e] = pack2<DT>(p0 - h.x, p1 - h.y);
+            for (int e = 0; e < 16; ++e) {
+              const bool k0 = (mw[q] >> (2 * e)) & 1u, k1 = (mw[q] >> (2 * e + 1)) & 1u;
+              const float p0 = k0 ? ex2_approx(__uint_as_float(x[2 * e]) - m_run) : 0.f;
+              const float p1 = k1 ? ex2_approx(__uint_as_float(x[2 * e + 1]) - m_run) : 0.f;
+              sum4[e & 3] += p0 + p1;
+              hi[e] = pack2<DT>(p0, p1);
+              const float2 h = unpack2<DT>(hi[e]);
+              lo[q][e] = pack2<DT>(p0 - h.x, p1 - h.y);
+            }
+            tmem_st16_nw(ts + 64 * set + 16 * q, hi);
           }
-          tmem_st16_nw(ts + 16 * q, hi);
-          tmem_st16_nw(ts + 64 + 16 * q, lo);
+          tmem_st16_nw(ts + 64 * set + 32, lo[0]);
+          tmem_st16_nw(ts + 64 * set + 48, lo[1]);
+          tmem_wait_st();
+          sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
         }
-        const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-        tmem_wait_st();
         l_run = __fmaf_rn(l_run, alpha, sum);
-        }  // wlive
-        // O's row times alpha before this unit's PV, once the previous PV is done (PV(gi - 2)
-        // is: this unit's QK waited for it, so parity tells the phases apart)
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
-          if (!(ok = wait(pvdone, (uint32_t)(gi - 1) & 1u))) break;
+        // PV(gi - 1) is waited for at every unit, before this unit's P is announced: its
+        // phase is then told apart from the others by parity (PV(gi - 2) is complete -- this
+        // unit's QK waited for it -- and PV(gi) cannot be issued yet), and at the end of a
+        // piece only PV(last) remains
+        if (gi >= 1) {
+          ok = __all_sync(0xffffffffu, ok && wait(pvdone, (uint32_t)(gi - 1) & 1u));
           tc_fence_after();
+        }
+        // this set's O columns times alpha before this unit's PV
+        const bool any_resc = __any_sync(0xffffffffu, resc);
+        if (j > 0 && ok && any_resc) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int q2 = 0; q2 < 2; ++q2) {
             uint32_t o[32];
-            const uint32_t ta = tmem_addr(tbase, 32 * qd, TM_O + 32 * q4);
+            const uint32_t ta = tmem_addr(tbase, 32 * qd, TM_O + 64 * set + 32 * q2);
             tmem_ld<32>(ta, o);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
@@ -611,45 +669,54 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
         // V rows that no row of the tile attends to -- keys past the tile's last position
         // (the tail of its last page) and pages outside the cache (read from another
-        // block) -- may hold anything, NaN bit patterns included: zeroed, so that their
-        // zero probabilities contribute 0
-        if (c * 128 + m > mp || !((vb >> (m / BLK)) & 1)) {
-          const uint32_t vr = smem_u32(sm + st * Lay::STAGE + Lay::KV) + m * 128;
+        // block) -- may hold anything, NaN bit patterns included: zeroed (each set one of
+        // the row's two 64-column blocks), so that their zero probabilities contribute 0
+        if (ok && (c * 128 + m > mp || !((vb >> (m / BLK)) & 1))) {
+          const uint32_t vr = smem_u32(sm + st * Lay::STAGE + Lay::KV + set * Lay::BOX) + m * 128;
 #pragma unroll
-          for (int cb = 0; cb < 2; ++cb)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) sts128_zero(vr + cb * Lay::BOX + 16 * e);
+          for (int e = 0; e < 8; ++e) sts128_zero(vr + 16 * e);
         }
         fence_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(pfull + par);
       }
-      if (!ok) break;
-      // ---- end of piece: output rows, or the partial state ----
-      // the piece's last two PVs, in order: the barrier's phases are told apart by parity
-      // alone, so the wait for PV(last) is sound only once PV(last - 1) is known complete
-      // (PV(last - 2) is: the last unit's QK waited for it)
-      if (gi >= 2 && !wait(pvdone, (uint32_t)(gi - 2) & 1u)) break;
-      if (!wait(pvdone, (uint32_t)(gi - 1) & 1u)) break;
-      tc_fence_after();
+      // ---- end of piece ----
+      // the next piece's query rows are loaded now; they go to tensor memory after the
+      // readout, once this piece's last QK is done
+      const bool more = pc.u1 < b1;
       const bool complete = pc.seg0 >= b0 && pc.u1 == pc.seg1;
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const int seg0 = pc.seg0, h = pc.h;
+      uint4 vq[16];
+      if (more) {
+        w.seek(a, pc.u1);
+        const PfPiece pn = pf_piece(w, pc.u1, b1);
+        const uint4 *src = q_src(w, pn);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) vq[e] = src ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
+      }
+      // PV(last) (PV(last - 1) was waited for in the last unit)
+      ok = __all_sync(0xffffffffu, ok && wait(pvdone, (uint32_t)(gi - 1) & 1u));
+      tc_fence_after();
+      lxb[set * 128 + m] = l_run;
+      named_bar_sync(1, 256);
+      const float l_tot = l_run + lxb[(set ^ 1) * 128 + m];
+      const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
       uint4 *dst = reinterpret_cast<uint4 *>(
-          a.out + ((int64_t)tok * a.Hq + (int64_t)pc.h * G + g) * PF_D);
+          a.out + ((int64_t)tok * a.Hq + (int64_t)h * G + g) * PF_D + 64 * set);
       // slot 0: the CTA's first piece (its segment began at or before the range), slot 1:
       // its last piece
-      float *slot = a.partials + (size_t)(2 * blockIdx.x + (pc.seg0 <= b0 ? 0 : 1)) * PF_SLOT;
+      float *slot = a.partials + (size_t)(2 * blockIdx.x + (seg0 <= b0 ? 0 : 1)) * PF_SLOT;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t x[32];
-        tmem_ld<32>(tmem_addr(tbase, 32 * qd, TM_O + 32 * q4), x);
+      for (int q2 = 0; q2 < 2 && ok; ++q2) {
+        uint32_t xo[32];
+        tmem_ld<32>(tmem_addr(tbase, 32 * qd, TM_O + 64 * set + 32 * q2), xo);
         if (complete) {
           if (rv) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float *f = reinterpret_cast<const float *>(x + 8 * e);
-              dst[4 * q4 + e] = make_uint4(pack2<DT>(f[0] * inv, f[1] * inv),
+              const float *f = reinterpret_cast<const float *>(xo + 8 * e);
+              dst[4 * q2 + e] = make_uint4(pack2<DT>(f[0] * inv, f[1] * inv),
                                            pack2<DT>(f[2] * inv, f[3] * inv),
                                            pack2<DT>(f[4] * inv, f[5] * inv),
                                            pack2<DT>(f[6] * inv, f[7] * inv));
@@ -657,57 +724,21 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) slot[256 + (32 * q4 + e) * 128 + m] = __uint_as_float(x[e]);
+          for (int e = 0; e < 32; ++e)
+            slot[256 + (64 * set + 32 * q2 + e) * 128 + m] = __uint_as_float(xo[e]);
         }
       }
-      if (!complete) {
+      if (ok && !complete && set == 0) {
         slot[m] = m_run;
-        slot[128 + m] = l_run;
+        slot[128 + m] = l_tot;
       }
       tc_fence_before();
-    }
-  } else {
-    // ------------------------------ query rows ------------------------------
-    // row m: query head h * G + g of token i0 + t, rotated at the token's position,
-    // times scale * log2(e), as hi + lo 16-bit parts (element d at column d / 2)
-    regs_dec<PF_REG_QUERY>();
-    const int qd = warp & 3;
-    const int m = 32 * qd + lane;
-    const int tr = m / G, g = m % G;
-    int piece = 0;
-    for (int u = b0; u < b1; ++piece) {
-      w.seek(a, u);
-      const PfPiece pc = pf_piece(w, u, b1);
-      const int i0 = w.t.y, nt = w.t.z;
-      const bool rv = tr < nt;
-      const int tok = i0 + tr;
-      // the prepared row (hi words then lo words) is loaded before the wait
-      const uint4 *src = reinterpret_cast<const uint4 *>(
-          a.qhl + ((int64_t)(rv ? tok : 0) * a.Hq + (int64_t)pc.h * G + g) * PF_D);
-      uint4 v[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] = rv ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
-      // the previous piece's QKs are done with the tensor-memory Q
-      if (piece > 0 && !wait(qfree, (uint32_t)(piece - 1) & 1u)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
-        // words 16 q8 .. 16 q8 + 15: hi columns for q8 < 4, lo columns after
-        uint32_t wv[16];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          wv[4 * e] = v[4 * q8 + e].x;
-          wv[4 * e + 1] = v[4 * q8 + e].y;
-          wv[4 * e + 2] = v[4 * q8 + e].z;
-          wv[4 * e + 3] = v[4 * q8 + e].w;
-        }
-        tmem_st16_nw(tmem_addr(tbase, 32 * qd, (q8 < 4 ? TM_QHI : TM_QLO) + 16 * (q8 & 3)), wv);
+      if (more) {
+        // this piece's QKs are done with the tensor-memory Q (its last S was read)
+        ok = ok && wait(qfree, (uint32_t)piece & 1u);
+        tc_fence_after();
+        if (ok) q_store(vq);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tq);
-      u = pc.u1;
     }
   }
 

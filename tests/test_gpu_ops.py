@@ -815,6 +815,20 @@ def test_paged_prefill_runs_bad_block_and_determinism():
     assert np.array_equal(got, again, equal_nan=True)
 
 
+def test_paged_prefill_many_pieces_per_cta():
+    # 1300 query tokens listed request by request: full tiles of 32 tokens (every row
+    # live), several pieces per CTA, so every piece transition -- the last PV of one piece,
+    # the next piece's query rows, the combine of cut segments -- runs many times
+    D, G, Hkv, dt, theta = 128, 4, 8, W.BF16, 5e5
+    kc, vc, bt, seq, pos, q = _prefill_grouped(D, G, dt, [20, 3], [700, 600], Hkv, seed=92)
+    status = status_tensor()
+    got = _run_prefill(kc, vc, bt, seq, pos, q, dt, theta, 1000, status=status)
+    assert status.item() == 0
+    want, st = oracle.paged_prefill(kc, vc, 1, q, seq, pos, bt, theta, dt, n_threads=16)
+    assert st == 0
+    assert_decode_close(got, want, "prefill, many pieces per CTA")
+
+
 def test_paged_prefill_ignores_nan_rows_past_the_context():
     # every cache row that no query token may attend to -- slots past each request's last
     # token, blocks of no request -- holds NaN bit patterns; request 1's first page of its
