@@ -574,10 +574,10 @@ __device__ __forceinline__ float *partial_slot(const DecodeArgs &a, int c, int s
 // row's and piece's m and l (the same address in all lanes) and the lane's
 // slice of the accumulator -- before using any of them, so a segment costs
 // one dependent round trip after the descriptor.
-template <int D, int G, int HG, int DT, int NR>
+template <int D, int G, int HG, int DT, int NR, int R = 4>
 __device__ void combine_rows(const DecodeArgs &a, const CtaRange &rg, const Piece &pc,
                              const int (&rows)[NR], int lane) {
-  constexpr int PF = partial_floats(G, D), SLOT = HG * PF, DPL = D / 32, R = 4;
+  constexpr int PF = partial_floats(G, D), SLOT = HG * PF, DPL = D / 32;
   const int cf = cta_of(pc.seg_start, rg), cl = cta_of(pc.seg_end - 1, rg);
   const int npc = cl - cf + 1;
   float A[NR][DPL], M[NR], Ls[NR];
@@ -641,7 +641,10 @@ __device__ void combine_rows(const DecodeArgs &a, const CtaRange &rg, const Piec
 // The combine pass: grid (segments, ceil(HG*G / COMBINE_WARPS)), one warp per
 // output row: CTA (s, y) takes segment s = (request, head group) and, if the
 // split-K ranges cut it, combines its rows COMBINE_WARPS*y .. +COMBINE_WARPS-1,
-// four pieces' loads in flight per round. Whether and where a segment was cut
+// R pieces' loads in flight per round: four by default (a larger combine cannot stay
+// resident beside the 16-bit split pass, measured 54.7 -> 56.1 us per layer at R = 12 on the
+// 70B-shaped batch), twelve for the int8 decode's two-block units (its 512-thread CTAs leave
+// no room beside them anyway, and fewer rounds pay: 64.4 -> 59.5 us). Whether and where a segment was cut
 // follows from the context lengths alone, which the split-K pass read after its
 // own dependency wait (before it let this grid start): that is worked out, and
 // the segment's partial-state lines are prefetched, before this grid waits for
@@ -660,7 +663,7 @@ __device__ void combine_rows(const DecodeArgs &a, const CtaRange &rg, const Piec
 // enqueued before the split-K pass has completed by then (the split-K pass
 // released this grid only after its own dependency wait).
 constexpr int COMBINE_WARPS = 8;
-template <int D, int G, int HG, int DT, int BPU, bool RELEASE_EARLY = false>
+template <int D, int G, int HG, int DT, int BPU, bool RELEASE_EARLY = false, int R = 4>
 __global__ void __launch_bounds__(COMBINE_WARPS * 32) decode_combine_kernel(DecodeArgs a) {
   extern __shared__ int comb_sm[];  // scratch[COMBINE_WARPS], pre[batch + 1]
   if constexpr (RELEASE_EARLY) griddep_launch_dependents();
@@ -698,7 +701,7 @@ __global__ void __launch_bounds__(COMBINE_WARPS * 32) decode_combine_kernel(Deco
   if constexpr (!RELEASE_EARLY) griddep_launch_dependents();
   if (row >= ROWS) return;
   const int rows[1] = {row};
-  combine_rows<D, G, HG, DT, 1>(a, rg, pc, rows, lane);
+  combine_rows<D, G, HG, DT, 1, R>(a, rg, pc, rows, lane);
 }
 
 // Launch `kern` on stream s as a programmatic dependent of the kernel launched
@@ -722,11 +725,11 @@ cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, c
 }
 
 // the combine pass for a split-K grid of `ctas` CTAs
-template <int D, int G, int HG, int DT, int BPU = 1, bool RELEASE_EARLY = false>
+template <int D, int G, int HG, int DT, int BPU = 1, bool RELEASE_EARLY = false, int R = 4>
 cudaError_t launch_combine(const DecodeArgs &a, int ctas, cudaStream_t s) {
   DecodeArgs c = a;
   c.ctas = ctas;
-  return launch_pdl(decode_combine_kernel<D, G, HG, DT, BPU, RELEASE_EARLY>,
+  return launch_pdl(decode_combine_kernel<D, G, HG, DT, BPU, RELEASE_EARLY, R>,
                     dim3(a.batch * (a.Hkv / HG), (HG * G + COMBINE_WARPS - 1) / COMBINE_WARPS),
                     dim3(COMBINE_WARPS * 32), (size_t)(COMBINE_WARPS + a.batch + 1) * sizeof(int),
                     s, c);

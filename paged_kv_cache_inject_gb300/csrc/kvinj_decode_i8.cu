@@ -711,7 +711,7 @@ cudaError_t launch_i8_cfg(const DecodeArgs &a, const CUtensorMap &tmK, const CUt
   }
   cudaError_t e = launch_pdl(kern, dim3(ctas), dim3(i8_threads<SW>()), smem, s, tmK, tmV, a);
   if (e != cudaSuccess) return e;
-  return launch_combine<128, G, HG, DT, BPU>(a, ctas, s);
+  return launch_combine<128, G, HG, DT, BPU, false, BPU == 2 ? 12 : 4>(a, ctas, s);
 }
 
 // three stages beside two V tiles and two Q tiles when they fit, else two stages and one Q

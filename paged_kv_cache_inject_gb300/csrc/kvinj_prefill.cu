@@ -471,8 +471,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         for (int j = 0; u < pc.u1; ++u, ++j, ++gi) {
           const int st = gi % PF_S;
           if (j == 0) {
-            // the previous piece's last PV before this piece's Q (whose query warps wait
-            // for that piece to end)
+            // the previous piece's last PV before this piece's Q (the softmax warps copy the
+            // new Q rows only after reading that piece's O out)
             if (pend >= 0 && !(ok = issue_pv(pend, pend_first))) break;
             pend = -1;
             if (!(ok = wait(tq, (uint32_t)piece & 1u))) break;
