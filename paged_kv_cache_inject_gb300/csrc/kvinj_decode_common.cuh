@@ -641,10 +641,10 @@ __device__ void combine_rows(const DecodeArgs &a, const CtaRange &rg, const Piec
 // The combine pass: grid (segments, ceil(HG*G / COMBINE_WARPS)), one warp per
 // output row: CTA (s, y) takes segment s = (request, head group) and, if the
 // split-K ranges cut it, combines its rows COMBINE_WARPS*y .. +COMBINE_WARPS-1,
-// R pieces' loads in flight per round: four by default (a larger combine cannot stay
-// resident beside the 16-bit split pass, measured 54.7 -> 56.1 us per layer at R = 12 on the
-// 70B-shaped batch), twelve for the int8 decode's two-block units (its 512-thread CTAs leave
-// no room beside them anyway, and fewer rounds pay: 64.4 -> 59.5 us). Whether and where a segment was cut
+// R pieces' loads in flight per round, CW warps per CTA: four and eight by default; with
+// two-block units (G = 8), whose segments span about twice as many ranges, twelve -- in CTAs
+// of four warps after the 16-bit split pass (so that they stay resident beside it), of eight
+// after the int8 decode (whose 512-thread CTAs leave no room beside them anyway). Whether and where a segment was cut
 // follows from the context lengths alone, which the split-K pass read after its
 // own dependency wait (before it let this grid start): that is worked out, and
 // the segment's partial-state lines are prefetched, before this grid waits for
@@ -663,13 +663,14 @@ __device__ void combine_rows(const DecodeArgs &a, const CtaRange &rg, const Piec
 // enqueued before the split-K pass has completed by then (the split-K pass
 // released this grid only after its own dependency wait).
 constexpr int COMBINE_WARPS = 8;
-template <int D, int G, int HG, int DT, int BPU, bool RELEASE_EARLY = false, int R = 4>
-__global__ void __launch_bounds__(COMBINE_WARPS * 32) decode_combine_kernel(DecodeArgs a) {
-  extern __shared__ int comb_sm[];  // scratch[COMBINE_WARPS], pre[batch + 1]
+template <int D, int G, int HG, int DT, int BPU, bool RELEASE_EARLY = false, int R = 4,
+          int CW = COMBINE_WARPS>
+__global__ void __launch_bounds__(CW * 32) decode_combine_kernel(DecodeArgs a) {
+  extern __shared__ int comb_sm[];  // scratch[CW], pre[batch + 1]
   if constexpr (RELEASE_EARLY) griddep_launch_dependents();
-  int *pre = comb_sm + COMBINE_WARPS;
+  int *pre = comb_sm + CW;
   const int ngrp = a.Hkv / HG;
-  unit_prefix<COMBINE_WARPS * 32>(a, pre, comb_sm,
+  unit_prefix<CW * 32>(a, pre, comb_sm,
                                   [&](int, int c) { return context_units<BPU>(a, c) * ngrp; });
   CtaRange rg;
   rg.Ptot = pre[a.batch];
@@ -681,7 +682,7 @@ __global__ void __launch_bounds__(COMBINE_WARPS * 32) decode_combine_kernel(Deco
   pc.seg_start = pre[pc.r] + pc.hg * pages;
   pc.seg_end = pc.seg_start + pages;
   constexpr int ROWS = HG * G, PF = partial_floats(G, D), SLOT = HG * PF;
-  const int row = blockIdx.y * COMBINE_WARPS + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int row = blockIdx.y * CW + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int cf = pages > 0 ? cta_of(pc.seg_start, rg) : 0;
   const int cl = pages > 0 ? cta_of(pc.seg_end - 1, rg) : 0;
   if (cf == cl) return;  // finished inside one split-K range (or empty)
@@ -725,13 +726,14 @@ cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, c
 }
 
 // the combine pass for a split-K grid of `ctas` CTAs
-template <int D, int G, int HG, int DT, int BPU = 1, bool RELEASE_EARLY = false, int R = 4>
+template <int D, int G, int HG, int DT, int BPU = 1, bool RELEASE_EARLY = false, int R = 4,
+          int CW = COMBINE_WARPS>
 cudaError_t launch_combine(const DecodeArgs &a, int ctas, cudaStream_t s) {
   DecodeArgs c = a;
   c.ctas = ctas;
-  return launch_pdl(decode_combine_kernel<D, G, HG, DT, BPU, RELEASE_EARLY, R>,
-                    dim3(a.batch * (a.Hkv / HG), (HG * G + COMBINE_WARPS - 1) / COMBINE_WARPS),
-                    dim3(COMBINE_WARPS * 32), (size_t)(COMBINE_WARPS + a.batch + 1) * sizeof(int),
+  return launch_pdl(decode_combine_kernel<D, G, HG, DT, BPU, RELEASE_EARLY, R, CW>,
+                    dim3(a.batch * (a.Hkv / HG), (HG * G + CW - 1) / CW),
+                    dim3(CW * 32), (size_t)(CW + a.batch + 1) * sizeof(int),
                     s, c);
 }
 

@@ -647,7 +647,11 @@ static cudaError_t launch_umma_cfg(const DecodeArgs &a, const CUtensorMap &tmK,
   }
   cudaError_t e = launch_pdl(kern, dim3(ctas), dim3(umma_threads<SW>()), smem, s, tmK, tmV, a);
   if (e != cudaSuccess) return e;
-  return launch_combine<128, G, HG, DT, BPU, UMMA_COMBINE_RELEASE_EARLY<EARLY, BPU>>(a, ctas, s);
+  // two-block units (G = 8): twelve pieces per round, in CTAs of four warps (small enough to
+  // stay resident beside the split pass at that round size)
+  constexpr int CR = BPU == 2 ? 12 : 4, CWN = BPU == 2 ? 4 : COMBINE_WARPS;
+  return launch_combine<128, G, HG, DT, BPU, UMMA_COMBINE_RELEASE_EARLY<EARLY, BPU>, CR, CWN>(
+      a, ctas, s);
 }
 
 // three stages when they fit beside the Q and P tiles, else two. G = 8 takes units of two
