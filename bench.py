@@ -194,9 +194,36 @@ def _traffic_from_profile(kernel_tag: str):
     return value if want_hash == src else None
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs collapsed to one space:
+    what the compiler sees, so that editing a comment or the layout keeps a summary valid.
+    String and character literals are kept as written (a "//" inside one is not a comment)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == "/" and text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif c == "/" and text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def _source_hash(kind: str = "") -> str:
-    """sha256 (16 hex digits) of the sources of one kernel kind (every file under csrc/
-    for an unknown kind)."""
+    """sha256 (16 hex digits) of the code of one kernel kind's sources, comments and
+    layout aside (every file under csrc/ for an unknown kind)."""
     csrc = os.path.join(ROOT, "paged_kv_cache_inject_gb300", "csrc")
     if kind in _KERNEL_SOURCES:
         names = sorted(set(_KERNEL_SOURCES[kind] + _COMMON_SOURCES))
@@ -204,7 +231,9 @@ def _source_hash(kind: str = "") -> str:
         names = sorted(n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h")))
     h = hashlib.sha256()
     for name in names:
-        h.update(open(os.path.join(csrc, name), "rb").read())
+        h.update(name.encode() + b"\0")
+        h.update(_code_only(open(os.path.join(csrc, name), encoding="utf-8").read()).encode())
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 

@@ -29,7 +29,10 @@
 //       memory-bound loop).
 //   softmax: warps 4..7 each own 32 rows of S (two heads, or one at G = 8),
 //       one row per thread; a head's tokens are TPH lanes, reduced with
-//       shuffles.
+//       shuffles. At G >= 2 warps 8..11 are a second set on the same rows:
+//       each set takes half of the query heads of every kv head (its own
+//       exponentials, P columns, O rescale and readout), and the two sets
+//       meet at one named barrier per unit.
 //   PV: O^T[128 x N] += V_unit^T[128 x 128] P^T[128 x N], where P^T is block
 //       diagonal: the column of query head (h, g) holds that head's 16
 //       probabilities in the rows of head h and zeros elsewhere, so each
@@ -55,12 +58,13 @@
 // attended token (context length minus the window); the softmax masks tokens before it as
 // it masks those past the context.
 //
-// Warp roles (256 threads):
+// Warp roles (256 threads, 384 with two softmax sets):
 //   warp 0     TMA producer (stages of K and V rows)
 //   warp 1     TMEM owner; lane 0 issues every MMA and commit
 //   warps 2-3  query preparation: rotate (RoPE at the request's position),
 //              scale, split hi/lo, write the swizzled Q tile of each piece
 //   warps 4-7  softmax, P tile, rescaling of O, end-of-piece output
+//   warps 8-11 (G >= 2) the second softmax set
 // Every wait is bounded; a wait that gives up sets the abort flag and
 // KVINJ_ST_TIMEOUT, later waits return at once, and all roles still reach
 // the final barrier, after which TMEM is released.

@@ -55,3 +55,13 @@ def test_a_stale_summary_reports_no_traffic(tmp_path, monkeypatch):
                tmp_path / "paged_kv_cache_inject_gb300" / "csrc")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench._traffic_from_profile(os.path.basename(src)[:-4]) is None
+
+
+def test_the_hash_follows_code_not_comments():
+    code = 'int f(int x) { return x + 1; }\nconst char *s = "a // b";\n'
+    commented = ('// a new comment\nint f(int x) {  /* inline */ return x + 1; }\n'
+                 'const char *s = "a // b";   // tail\n')
+    assert bench._code_only(code) == bench._code_only(commented)
+    assert bench._code_only(code) != bench._code_only(code.replace("x + 1", "x + 2"))
+    # a comment marker inside a string literal is code
+    assert bench._code_only('s = "/* x */";') != bench._code_only('s = "";')
