@@ -28,7 +28,7 @@
  *   [KM]  "Latency Optimization > KV Cache Management" -- size_KV formula;
  *         pages of 16 tokens read through a page table.
  *
- * Readings where the pages are silent (each listed in the design notes):
+ * Readings where the pages are silent:
  *   - RoPE pairing is rotate-half (i, i + D/2), the convention of the
  *     apply_rotary_pos_emb function [IS §3.1] names; inv_freq_i =
  *     theta^(-2i/D); angle = position * inv_freq_i; all in fp64 (libm).

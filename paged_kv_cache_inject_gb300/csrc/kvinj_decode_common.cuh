@@ -638,22 +638,22 @@ __device__ void combine_rows(const DecodeArgs &a, const CtaRange &rg, const Piec
   }
 }
 
-// The combine pass: grid (segments, ceil(HG*G / COMBINE_WARPS)), one warp per
-// output row: CTA (s, y) takes segment s = (request, head group) and, if the
-// split-K ranges cut it, combines its rows COMBINE_WARPS*y .. +COMBINE_WARPS-1,
-// R pieces' loads in flight per round, CW warps per CTA: four and eight by default; with
-// two-block units (G = 8), whose segments span about twice as many ranges, twelve -- in CTAs
-// of four warps after the 16-bit split pass (so that they stay resident beside it), of eight
-// after the int8 decode (whose 512-thread CTAs leave no room beside them anyway). Whether and where a segment was cut
-// follows from the context lengths alone, which the split-K pass read after its
-// own dependency wait (before it let this grid start): that is worked out, and
-// the segment's partial-state lines are prefetched, before this grid waits for
-// the split-K pass. A grid of segments (a few per SM at serving batch sizes)
-// leaves its CTAs resident beside the decode CTAs, so only the loads of the
-// partial states follow the wait. (Measured at batch 32, split-K pass +
-// combine per layer: one CTA per segment with two rows per warp 50.5 us; one
-// warp per row over a grid of decode CTAs 42.9 us; this grid of segments: see
-// the design notes.)
+// The combine pass: grid (segments, ceil(HG*G / CW)), CW warps per CTA, one warp
+// per output row: CTA (s, y) takes segment s = (request, head group) and, if the
+// split-K ranges cut it, combines its rows CW*y .. CW*y + CW - 1, R pieces' loads
+// in flight per round. By default R = 4 and CW = 8; with two-block units (G = 8),
+// whose segments span about twice as many ranges, R = 12 -- in CTAs of four warps
+// after the 16-bit split pass (so that they stay resident beside it), of eight
+// after the int8 decode (whose 512-thread CTAs leave no room beside them anyway).
+// Whether and where a segment was cut follows from the context lengths alone,
+// which the split-K pass read after its own dependency wait (before it let this
+// grid start): that is worked out, and the segment's partial-state lines are
+// prefetched, before this grid waits for the split-K pass. A grid of segments (a
+// few per SM at serving batch sizes) leaves its CTAs resident beside the decode
+// CTAs, so only the loads of the partial states follow the wait. (Measured at
+// batch 32, split-K pass + combine per layer: one CTA per segment with two rows
+// per warp 50.5 us; one warp per row over a grid of decode CTAs 42.9 us; one warp
+// per row over this grid of segments 41.2 us.)
 //
 // RELEASE_EARLY: the kernel after this one is released at this pass's start
 // instead of after its dependency wait. That kernel still waits for this grid's
