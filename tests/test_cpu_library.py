@@ -130,6 +130,9 @@ def test_prefill_host_validation(lib):
     # no GPU needed: sizes and argument checks happen before any launch
     assert lib.kvinj_prefill_workspace_size(0, 32, 8, 128, 64) == 0
     assert lib.kvinj_prefill_workspace_size(10, 30, 8, 128, 64) == 0  # Hq not a multiple of Hkv
+    assert lib.kvinj_prefill_workspace_size(10, 32, 0, 128, 64) == 0  # no kv heads
+    assert lib.kvinj_prefill_workspace_size(10, 0, 8, 128, 64) == 0  # no query heads
+    assert lib.kvinj_prefill_workspace_size(10, 32, 8, 128, 0) == 0  # no table columns
     r = lambda x: (x + 255) // 256 * 256
     # tensor-core path (D = 128, G in {1, 2, 4, 8}): a header, 16 bytes of tile and 4 of
     # unit prefix per query token, per-CTA entries that do not depend on the tokens, and
