@@ -107,6 +107,14 @@ def test_host_validation_rejects_before_launch(lib):
                                   None, None) == K.KVINJ_EUNSUPPORTED
     assert lib.kvinj_paged_decode(r(cache), None, 0, 12, 16, 16, 16, 4, 16, 1, 0.0, 16, 16, 1 << 30,
                                   None, None) == K.KVINJ_EINVAL
+    # decode: an empty batch is a no-op; batches beyond the prefix sums' shared memory and
+    # windows on the other kernels are refused
+    assert lib.kvinj_paged_decode(r(cache), None, 0, 32, None, None, None, 4, None, 0, 0.0, None,
+                                  None, 0, None, None) == K.KVINJ_OK
+    assert lib.kvinj_paged_decode(r(cache), None, 0, 32, 16, 16, 16, 4, 16, 5000, 0.0, 16, 16,
+                                  1 << 40, None, None) == K.KVINJ_EUNSUPPORTED
+    assert lib.kvinj_paged_decode(r(cache), None, 0, 32, 16, 16, 16, 4, 16, -1, 0.0, 16, 16,
+                                  1 << 30, None, None) == K.KVINJ_EINVAL
     # decode with rope but no q_pos
     assert lib.kvinj_paged_decode(r(cache), r(rope), 0, 32, 16, None, 16, 4, 16, 1, 0.0, 16, 16,
                                   1 << 30, None, None) == K.KVINJ_EINVAL
