@@ -12,6 +12,13 @@
  *                       the request's non-contiguous blocks (split-K over the
  *                       context, online softmax, in-kernel combine)
  *
+ * and around them: the append fused into the decode (kvinj_append_paged_decode),
+ * a sliding-window decode (kvinj_paged_decode_window), block copies for
+ * copy-on-write (kvinj_copy_blocks), the paged prefill of query tokens
+ * (kvinj_paged_prefill), an int8 cache (kvinj_inject_i8, kvinj_append_i8,
+ * kvinj_paged_decode_i8), and a decode with no caller workspace
+ * (kvinj_paged_decode_static).
+ *
  * Sources (web pages, by title and section):
  *   "InferScale: GPU-Native KV Injection for Personalized LLM Serving":
  *     §2.3 RoPE, R_a^T R_b = R_{b-a}; §3.1 keys stored before RoPE;
@@ -27,10 +34,13 @@
  *
  * Conventions (all entry points):
  *   - Every array pointer is a DEVICE pointer owned by the caller, except the
- *     output of kvinj_rope_table_host (host memory). The library allocates and
- *     frees nothing, keeps no global state, and never synchronises: each call
- *     enqueues its kernels on `stream` (NULL = legacy default stream) and
- *     returns. Results are visible to later work on the same stream.
+ *     outputs of kvinj_rope_table_host / kvinj_rope_table64_host (host memory)
+ *     and a chunk pool in page-locked host memory. The library allocates and
+ *     frees nothing and keeps no global state (the one exception is the fixed
+ *     device scratch array of kvinj_paged_decode_static), and never
+ *     synchronises: each call enqueues its kernels on `stream` (NULL = legacy
+ *     default stream) and returns. Results are visible to later work on the
+ *     same stream.
  *   - Return value: KVINJ_OK, or an error code for arguments the host can see
  *     are wrong (nothing is launched then), or KVINJ_ECUDA when a launch fails.
  *   - Bad indices that only the device sees (chunk id, slot, block-table
@@ -38,7 +48,8 @@
  *     decode page with a bad block is treated as masked) and a KVINJ_ST_* bit
  *     is OR-ed into *dev_status (a caller-owned device int32; may be NULL).
  *   - Element types: 16-bit floats (bf16 or fp16), the same type for pool,
- *     cache, queries and outputs. Pointers to 16-bit data must be 16-byte
+ *     cache, queries and outputs (an int8 cache holds codes and fp32 scales
+ *     instead; see kvinj_cache_i8). Pointers to 16-bit data must be 16-byte
  *     aligned.
  *   - Layouts (row-major, innermost last):
  *       pool   [num_chunks][L][2 (K, V)][chunk_len][Hkv][D]   keys pre-RoPE
