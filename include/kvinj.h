@@ -394,10 +394,10 @@ int kvinj_append_paged_decode_ex(const kvinj_cache *cache, const kvinj_rope *rop
  * shapes return KVINJ_EWORKSPACE.
  * Every call looks up the array's device address in the current context (it
  * is not cached, so a device reset cannot leave a stale address behind); the
- * first call on a device may load the library's device code there, so make
- * it before any stream capture. All calls on a device share the array and
- * leave their contents in it; nothing in it needs to start at zero, but calls
- * whose kernels overlap on the GPU race on it. */
+ * first call on a device may load the library's device code there. All calls
+ * on a device share the array and leave their contents in it; nothing in it
+ * needs to start at zero, but calls whose kernels overlap on the GPU race on
+ * it. */
 #define KVINJ_STATIC_SCRATCH_BYTES (24u << 20)
 int kvinj_paged_decode_static(const kvinj_cache *cache, const kvinj_rope *rope, int32_t layer,
                               int32_t num_q_heads, const void *q, const int32_t *q_pos,

@@ -20,7 +20,7 @@
 // device's primary context is destroyed and recreated, the module is loaded
 // again and the array may sit elsewhere, and a cached address would point at
 // freed memory. The first call on a device loads this library's device code
-// there if nothing else has, so make it before any stream capture.
+// there if nothing else has.
 //
 // Sharing: every call on a device uses the same array and leaves the last
 // call's contents there. Nothing in it needs to start at zero (each call
